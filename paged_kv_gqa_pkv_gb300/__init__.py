@@ -1,0 +1,9 @@
+"""GB300-native attention over a paged KV cache.
+
+The compute lives in ``libpkv.so`` (hand-written CUDA for sm_103a, C ABI
+declared in ``include/pkv.h``). ``paged_kv_gqa_pkv_gb300.binding`` is the thin
+ctypes layer over it; ``paged_kv_gqa_pkv_gb300.workloads`` draws seeded
+synthetic inputs.
+"""
+
+__all__ = ["binding", "workloads"]

@@ -1,0 +1,172 @@
+"""Power of the oracle pins: each test plants one plausible mistake in a copy
+of an oracle function (on the CPU) and requires that some pin fails.
+
+A mistake that no pin catches would mean the pins cannot vouch for the
+oracle, so every planted mistake here must be caught."""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle.paged_attention as orc
+from tests import oracle_pins
+
+
+def _caught(monkeypatch, name, fn):
+    monkeypatch.setattr(orc, name, fn)
+    failures = []
+    for check in oracle_pins.ALL_CHECKS:
+        try:
+            check(orc)
+        except Exception as e:  # noqa: BLE001 - any failure counts as caught
+            failures.append((check.__name__, type(e).__name__))
+    return failures
+
+
+def _attend_variant(head_map=None, use_scale=True, add_max=True, swap_kv=False,
+                    drop_last=False):
+    def attend(q, K, V, scale):
+        hq, d = q.shape
+        n = K.shape[0] - (1 if drop_last and K.shape[0] > 1 else 0)
+        out = np.zeros((hq, d))
+        lse = np.full((hq,), -np.inf)
+        if n == 0:
+            return out, lse
+        hkv = K.shape[1]
+        g = hq // hkv
+        for h in range(hq):
+            kvh = head_map(h, g, hkv) if head_map else h // g
+            KK, VV = (V, K) if swap_kv else (K, V)
+            s = (scale if use_scale else 1.0) * (KK[:n, kvh, :] @ q[h])
+            m = np.max(s)
+            lse[h] = (m if add_max else 0.0) + math.log(np.sum(np.exp(s - m)))
+            p = np.exp(s - (m + math.log(np.sum(np.exp(s - m)))))
+            out[h] = p @ VV[:n, kvh, :]
+        return out, lse
+    return attend
+
+
+MUTANTS = {
+    "gqa_head_modulo": ("attend", _attend_variant(head_map=lambda h, g, hkv: h % hkv)),
+    "no_scale": ("attend", _attend_variant(use_scale=False)),
+    "lse_without_max": ("attend", _attend_variant(add_max=False)),
+    "k_v_swapped": ("attend", _attend_variant(swap_kv=True)),
+    "last_key_dropped": ("attend", _attend_variant(drop_last=True)),
+}
+
+
+def _physical_slot_swapped(page_table, slot, pos, page_size, num_pages):
+    if slot < 0 or slot >= page_table.shape[0] or pos < 0:
+        return None
+    block = pos % page_size                 # planted: block and offset swapped
+    if block >= page_table.shape[1]:
+        return None
+    page = int(page_table[slot, block])
+    if page < 0 or page >= num_pages:
+        return None
+    return page * page_size + pos // page_size
+
+
+def _physical_slot_no_range_check(page_table, slot, pos, page_size, num_pages):
+    page = int(page_table[slot, pos // page_size])
+    return page * page_size + pos % page_size   # planted: -1 not rejected
+
+
+def _append_writes_padding(k_pool, v_pool, page_table, k_new, v_new, batch_idx,
+                           input_pos, page_size):
+    k_out, v_out = k_pool.copy(), v_pool.copy()
+    P = k_out.shape[0] // page_size
+    bad = []
+    for i in range(len(batch_idx)):
+        r = orc.physical_slot(page_table, int(batch_idx[i]), int(input_pos[i]),
+                              page_size, P)
+        if r is None:
+            if int(batch_idx[i]) != 0:
+                bad.append(i)
+            continue
+        k_out[r] = k_new[i]             # planted: slot 0 rows are written too
+        v_out[r] = v_new[i]
+    return k_out, v_out, bad
+
+
+_real_decode = orc.decode_attention
+_real_prefill = orc.prefill_attention
+_real_round = orc.f64_to_bf16_bits
+
+
+def _decode_off_by_one(q, kp, vp, table, bidx, lens, ps, scale, rows=None):
+    return _real_decode(q, kp, vp, table, bidx, np.asarray(lens) - 1, ps, scale, rows)
+
+
+def _decode_nan_on_empty(q, kp, vp, table, bidx, lens, ps, scale, rows=None):
+    out, lse, bad = _real_decode(q, kp, vp, table, bidx, lens, ps, scale, rows)
+    empty = (np.asarray(bidx) == 0) | (np.asarray(lens) <= 0)
+    out[empty] = np.nan                  # planted: empty rows give NaN
+    return out, lse, bad
+
+
+def _decode_ignores_slot(q, kp, vp, table, bidx, lens, ps, scale, rows=None):
+    # planted: row b reads slot b+1 instead of batch_idx[b]
+    return _real_decode(q, kp, vp, table, np.arange(1, len(bidx) + 1), lens,
+                        ps, scale, rows)
+
+
+def _prefill_strict_causal(q, k, v, bidx, pos, scale, rows=None):
+    # planted: keys with pos < pos_i only (the diagonal is dropped); done by
+    # shifting every query position down by one within its document
+    return _real_prefill(q, k, v, bidx, np.asarray(pos), scale, rows) \
+        if False else _strict(q, k, v, bidx, pos, scale)
+
+
+def _strict(q, k, v, bidx, pos, scale):
+    T, hq, d = q.shape
+    out = np.zeros((T, hq, d))
+    lse = np.full((T, hq), -np.inf)
+    qf, kf, vf = (orc.bf16_bits_to_f64(x) for x in (q, k, v))
+    for i in range(T):
+        if bidx[i] == 0:
+            continue
+        keys = np.nonzero((bidx == bidx[i]) & (pos < pos[i]))[0]
+        out[i], lse[i] = orc.attend(qf[i], kf[keys], vf[keys], scale)
+    return out, lse
+
+
+def _prefill_across_documents(q, k, v, bidx, pos, scale, rows=None):
+    # planted: the document boundary is ignored (plain causal over the packing)
+    T = len(bidx)
+    return _real_prefill(q, k, v, np.where(np.asarray(bidx) != 0, 1, 0),
+                         np.arange(T), scale, rows)
+
+
+def _round_truncate(x):
+    x = np.asarray(x, dtype=np.float64)
+    return (x.astype(np.float32).view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+def _round_via_f32(x):
+    x = np.asarray(x, dtype=np.float64)
+    import torch
+    t = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+MUTANTS.update({
+    "page_formula_swapped": ("physical_slot", _physical_slot_swapped),
+    "unreserved_page_accepted": ("physical_slot", _physical_slot_no_range_check),
+    "append_writes_padding_slot": ("append", _append_writes_padding),
+    "decode_seq_len_off_by_one": ("decode_attention", _decode_off_by_one),
+    "decode_empty_rows_nan": ("decode_attention", _decode_nan_on_empty),
+    "decode_ignores_batch_idx": ("decode_attention", _decode_ignores_slot),
+    "prefill_strict_causal": ("prefill_attention", _prefill_strict_causal),
+    "prefill_ignores_documents": ("prefill_attention", _prefill_across_documents),
+    "bf16_truncation": ("f64_to_bf16_bits", _round_truncate),
+    "bf16_double_rounding": ("f64_to_bf16_bits", _round_via_f32),
+})
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS))
+def test_planted_mistake_is_caught(monkeypatch, mutant):
+    name, fn = MUTANTS[mutant]
+    failures = _caught(monkeypatch, name, fn)
+    assert failures, f"no pin caught the planted mistake {mutant!r}"
