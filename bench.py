@@ -1,0 +1,444 @@
+"""Benchmark: one decode step of a paged-KV GQA attention layer, Qwen3-4B shape.
+
+A step is the whole hot path on one batch: ``pkv_append`` of the 64 new
+tokens' K/V through the page table, then ``pkv_decode_attention`` (split-KV
+pass over the pages + LSE merge). Workload: B=64, Hq=32, Hkv=8, D=128,
+page 128, keys attended uniform in [512, 1024], sequential pages (a fresh
+batch's allocation, the contiguous fast path); a second line of numbers is
+taken with randomly permuted pages, and the packed document-causal prefill
+(64 documents, lengths uniform in [64, 1024]) is timed alongside.
+
+Inputs are seeded synthetic tensors (the pages measured real prompts of a
+public math dataset; these stand in with the same shapes and lengths).
+Timing: CUDA events on the launching stream; the K timed steps rotate over
+enough independent pool sets that the KV read each step (~201 MB) comes from
+HBM, not L2. Prints one JSON line on rank 0.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkv|reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn KV GB/s & % of HBM peak; tokens/s/layer at B=64 Qwen3-4B shape"
+UNIT = "GB/s"
+WORKLOAD = ("qwen3_b64_decode: B=64, Hq=32, Hkv=8, D=128, page_size=128, keys U[512,1024], "
+            "sequential pages, seed 0; step = append 64 tokens + split-KV decode")
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES = 126 * 1024 * 1024
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def decode_bytes(case) -> int:
+    """Algorithmic bytes of one decode launch: K and V rows of every attended
+    key (all kv heads), q in, out and lse out, the page-table entries walked,
+    batch_idx and seq_lens."""
+    d = case.head_dim
+    hkv, hq, B = case.num_kv_heads, case.num_q_heads, case.batch
+    live = case.batch_idx != 0
+    lens = case.seq_lens[live].long()
+    kv = int(lens.sum()) * hkv * d * 2 * 2
+    pages = int(((lens + case.page_size - 1) // case.page_size).sum()) * 4
+    return kv + B * hq * d * 2 * 2 + B * hq * 4 + pages + B * 8
+
+
+def append_bytes(case) -> int:
+    n = int((case.batch_idx != 0).sum())
+    return n * case.num_kv_heads * case.head_dim * 2 * 2 * 2 + case.batch * 8 + n * 4
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+_ORACLE_CHILD = """
+import json, statistics, sys, time
+sys.path.insert(0, ROOT)
+import oracle.paged_attention as orc
+from paged_kv_gqa_pkv_gb300 import workloads as W
+from paged_kv_gqa_pkv_gb300.workloads import bf16_bits
+c = W.qwen3_b64_decode(0, permute=False)
+kb, vb = bf16_bits(c.k_pool), bf16_bits(c.v_pool)
+tab, bi, ip, sl = (c.page_table.numpy(), c.batch_idx.numpy(), c.input_pos.numpy(),
+                   c.seq_lens.numpy())
+kn, vn, q = bf16_bits(c.k_new), bf16_bits(c.v_new), bf16_bits(c.q)
+row_kv = [int(n) * c.num_kv_heads * c.head_dim * 4 for n in sl]
+res = {}
+if MODE == "full":
+    # whole step: append of the 64 new tokens, then decode of all 64 rows
+    times = []
+    for _ in range(REPS):
+        t0 = time.perf_counter()
+        k2, v2, _ = orc.append(kb, vb, tab, kn, vn, bi, ip, c.page_size)
+        orc.decode_attention(q, k2, v2, tab, bi, sl, c.page_size, c.scale)
+        times.append(time.perf_counter() - t0)
+    res = {"seconds": statistics.median(times), "kv_bytes": sum(row_kv)}
+else:
+    # one row per step (row i % 64), pools already holding the appended tokens
+    k2, v2, _ = orc.append(kb, vb, tab, kn, vn, bi, ip, c.page_size)
+    tot_t, tot_b = 0.0, 0
+    for i in range(WARMUP + STEPS):
+        r = i % c.batch
+        t0 = time.perf_counter()
+        orc.decode_attention(q, k2, v2, tab, bi, sl, c.page_size, c.scale, rows=[r])
+        dt = time.perf_counter() - t0
+        if i >= WARMUP:
+            tot_t += dt
+            tot_b += row_kv[r]
+    res = {"seconds": tot_t, "kv_bytes": tot_b, "steps": STEPS}
+print(json.dumps(res))
+"""
+
+
+def run_oracle_child(mode: str, reps: int = 5, steps: int = 0, warmup: int = 0):
+    """Runs the oracle, as it stands, in a child process with one BLAS thread
+    (started by subprocess, never forked from a process that touched CUDA)."""
+    code = (f"ROOT={ROOT!r}\nMODE={mode!r}\nREPS={reps}\nSTEPS={steps}\n"
+            f"WARMUP={warmup}\n") + _ORACLE_CHILD
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1",
+               MKL_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=3600)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return d["kv_bytes"] / d["seconds"] / 1e9, d
+
+
+def run_reference(args):
+    """Reference arm: the float64 CPU oracle on the same workload, metric and
+    unit; each step is a bounded sample (one of the 64 rows, in turn)."""
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    value, d = run_oracle_child("rows", steps=args.steps, warmup=args.warmup)
+    sample = "decode of one row per step (row = step mod 64), append done before timing"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": d["seconds"] / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_pkv(args):
+    import torch
+    from paged_kv_gqa_pkv_gb300 import binding
+    from paged_kv_gqa_pkv_gb300 import build as _b
+    from paged_kv_gqa_pkv_gb300 import workloads as W
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        _b.build()
+    if world > 1:
+        dist.barrier()
+    binding.load_library()
+    hbm_peak, bf16_peak, peak_kind = _peaks()
+    stream = torch.cuda.current_stream()
+
+    def make_sets(case, n_sets):
+        sets = []
+        for _ in range(n_sets):
+            sets.append(dict(
+                kp=case.k_pool.to(dev), vp=case.v_pool.to(dev), pt=case.page_table.to(dev),
+                q=case.q.to(dev), kn=case.k_new.to(dev), vn=case.v_new.to(dev),
+                bi=case.batch_idx.to(dev), ip=case.input_pos.to(dev),
+                sl=case.seq_lens.to(dev)))
+        return sets
+
+    def kv_set_bytes(case):
+        return 2 * case.k_pool.numel() * 2
+
+    def timed_decode(case, steps, warmup):
+        """Times `steps` decode steps (append + decode) replayed from CUDA
+        graphs, rotating over pool sets so each step's KV comes from HBM; a
+        second graph of decode calls alone gives the decode call's duration."""
+        n_sets = max(2, math.ceil(2 * L2_BYTES / kv_set_bytes(case)) + 1)
+        sets = make_sets(case, n_sets)
+        B, hq = case.batch, case.num_q_heads
+        ws_bytes = binding.pkv_decode_workspace_size(sets[0]["kp"], sets[0]["pt"],
+                                                     case.page_size, B, hq)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        out = torch.empty((B, hq, 128), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((B, hq), dtype=torch.float32, device=dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def append(i):
+            s = sets[i % n_sets]
+            binding.pkv_append(s["kp"], s["vp"], s["pt"], s["kn"], s["vn"], s["bi"], s["ip"],
+                               case.page_size, dev_err=err)
+
+        def decode(i):
+            s = sets[i % n_sets]
+            binding.pkv_decode_attention(s["kp"], s["vp"], s["pt"], s["q"], s["bi"], s["sl"],
+                                         case.page_size, case.scale, out=out, lse=lse,
+                                         workspace=ws, dev_err=err)
+
+        for i in range(max(warmup, n_sets)):   # eager warm-up (first-call set-up)
+            append(i)
+            decode(i)
+        torch.cuda.synchronize()
+
+        per_graph = n_sets * max(1, 96 // n_sets)
+
+        def capture(n, body):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for i in range(n):
+                    body(i)
+            return g
+
+        step_g = capture(per_graph, lambda i: (append(i), decode(i)))
+        tail = steps % per_graph
+        tail_g = capture(tail, lambda i: (append(i), decode(i))) if tail else None
+        dec_g = capture(per_graph, decode)
+        for _ in range(max(1, warmup // per_graph)):
+            step_g.replay()
+            dec_g.replay()
+        torch.cuda.synchronize()
+
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        with ClockSampler(local) as clk:
+            t0.record()
+            for _ in range(steps // per_graph):
+                step_g.replay()
+            if tail_g is not None:
+                tail_g.replay()
+            t1.record()
+            torch.cuda.synchronize()
+        total_ms = t0.elapsed_time(t1)
+
+        # decode calls alone, same graph shape; several timed replays
+        reps = max(3, min(50, steps // per_graph))
+        dec_ms = []
+        for _ in range(reps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            dec_g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            dec_ms.append(a.elapsed_time(b) / per_graph)
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(err.item()):#x} during the bench")
+        dec_sorted = sorted(dec_ms)
+        return dict(total_ms=total_ms, dec_ms=statistics.median(dec_ms),
+                    dec_p10=dec_sorted[len(dec_ms) // 10],
+                    dec_p90=dec_sorted[(9 * len(dec_ms)) // 10],
+                    clocks=clk.summary(), n_sets=n_sets, set_bytes=kv_set_bytes(case),
+                    per_graph=per_graph)
+
+    def e2e_decode(case, steps, warmup):
+        """Same step through the public binding with pinned host buffers: each
+        step copies its inputs host->device and reads the result back."""
+        s = make_sets(case, 1)[0]
+        host = {k: getattr(case, a).pin_memory() for k, a in
+                (("q", "q"), ("kn", "k_new"), ("vn", "v_new"), ("bi", "batch_idx"),
+                 ("ip", "input_pos"), ("sl", "seq_lens"), ("pt", "page_table"))}
+        B, hq = case.batch, case.num_q_heads
+        out_h = torch.empty((B, hq, 128), dtype=torch.bfloat16).pin_memory()
+        lse_h = torch.empty((B, hq), dtype=torch.float32).pin_memory()
+        ws = torch.empty(binding.pkv_decode_workspace_size(s["kp"], s["pt"], case.page_size,
+                                                           B, hq),
+                         dtype=torch.uint8, device=dev)
+        out = torch.empty((B, hq, 128), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((B, hq), dtype=torch.float32, device=dev)
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_h.numel() * 2 + lse_h.numel() * 4
+
+        def step():
+            for k, t in host.items():
+                s[k].copy_(t, non_blocking=True)
+            binding.pkv_append(s["kp"], s["vp"], s["pt"], s["kn"], s["vn"], s["bi"], s["ip"],
+                               case.page_size, stream=stream)
+            binding.pkv_decode_attention(s["kp"], s["vp"], s["pt"], s["q"], s["bi"], s["sl"],
+                                         case.page_size, case.scale, out=out, lse=lse,
+                                         workspace=ws, stream=stream)
+            out_h.copy_(out, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(warmup):
+            step()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for _ in range(steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / steps, h2d, d2h
+
+    case = W.qwen3_b64_decode(0, permute=False)
+    bytes_dec = decode_bytes(case)
+    kv_only = int(case.seq_lens.long().sum()) * case.num_kv_heads * case.head_dim * 4
+    r = timed_decode(case, args.steps, args.warmup)
+    ms_step = r["total_ms"] / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = world * kv_only / (ms_step * 1e-3) / 1e9
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    achieved = bytes_dec / (r["dec_ms"] * 1e-3) / 1e9
+    perm = W.qwen3_b64_decode(0, permute=True)
+    rp = timed_decode(perm, max(args.steps // 4, 10), args.warmup)
+    e2e_ms, h2d, d2h = e2e_decode(case, max(args.steps // 10, 10), args.warmup)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": f"inputs larger than L2: {r['n_sets']} rotating pool sets of "
+                         f"{r['set_bytes'] / 1e6:.0f} MB"},
+        "tokens_per_s_per_layer": world * case.batch / (ms_step * 1e-3),
+        "decode_call_us": r["dec_ms"] * 1e3, "decode_call_us_p10_p90": [r["dec_p10"] * 1e3,
+                                                                         r["dec_p90"] * 1e3],
+        "append_call_us_est": (ms_step - r["dec_ms"]) * 1e3,
+        "timing": f"CUDA-graph replay of {r['per_graph']}-step graphs; decode call = replay "
+                  f"of {r['per_graph']} decode calls / {r['per_graph']}",
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None,
+                     "kernel": "pkv_decode_attention (split-KV pass + LSE merge)",
+                     "peak_kind": peak_kind, "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS},
+        "permuted_pages": {"decode_call_us": rp["dec_ms"] * 1e3,
+                           "achieved_gbs": decode_bytes(perm) / (rp["dec_ms"] * 1e-3) / 1e9,
+                           "frac": decode_bytes(perm) / (rp["dec_ms"] * 1e-3) / 1e9 / hbm_peak},
+        "e2e": {"value": kv_only / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": 3 * args.steps,
+        "clocks": r["clocks"],
+    }
+    if not args.no_cpu_baseline:
+        gbs, d = run_oracle_child("full", reps=5)
+        line["cpu_baseline"] = {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": "the full step (append 64 tokens + decode all 64 "
+                                          "rows), median of 5, one BLAS thread",
+                                "seconds_per_step": d["seconds"]}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["pkv", "reference"], default="pkv")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_pkv(args)
+
+
+if __name__ == "__main__":
+    main()

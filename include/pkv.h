@@ -1,0 +1,184 @@
+/*
+ * pkv.h - C ABI of libpkv: attention over a paged KV cache on GB300 (sm_103a).
+ *
+ * The KV cache of one attention layer is one contiguous physical pool per
+ * tensor, K and V, each bf16 [num_pages * page_size, H_kv, D] (token-major,
+ * row-major, contiguous). A page table, int32 [max_batch, max_blocks]
+ * row-major, maps (batch slot, logical block) to a physical page. Batch slot 0
+ * and page 0 are reserved as no-op padding; an entry of -1 means "no page
+ * reserved". Source: "flex_paged_attention.py" commit log, section "Why this
+ * works", items 1 and 3.
+ *
+ * Three stream-ordered calls replace the pages' PagedKVCache.update followed
+ * by flex_attention(q, k, v, scale, block_mask, enable_gqa=True)
+ * ("qwen3_flex_inference.py", attention forward, _decode_step_eager,
+ * _prefill):
+ *   pkv_append            - write new tokens' K/V rows through the page table
+ *   pkv_decode_attention  - one query token per row, GQA, over the pages
+ *   pkv_prefill_attention - packed document-causal attention over fresh k/v
+ *
+ * Conventions for every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller. The library
+ *    keeps no pointer after the call returns and allocates no device memory;
+ *    scratch space, where needed, is a caller-provided workspace.
+ *  - Arguments are validated on the host, synchronously, before anything is
+ *    launched; a failed check returns its status and launches nothing.
+ *  - Problems only visible on the device (a page entry outside [0, num_pages),
+ *    a slot outside [0, max_batch), a position past the table) never trap:
+ *    the affected work is skipped and a PKV_DEV_ERR_* bit is OR-ed into the
+ *    optional int32 word dev_err (device memory, may be NULL). The caller
+ *    reads it after synchronising the stream. Results of affected rows are
+ *    unspecified; everything else is still computed.
+ *  - Calls only enqueue work on `stream` (NULL = the legacy default stream),
+ *    never synchronise it, and keep no state between calls, so they may be
+ *    captured into a CUDA graph.
+ *  - head_dim must be 128; num_q_heads / num_kv_heads (the GQA group) must be
+ *    1, 2, 4 or 8; page_size must be a positive multiple of 16; bf16 tensors
+ *    must be 16-byte aligned; int32/fp32 arrays 4-byte aligned.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_ARG = 1,        /* bad size, null pointer or unsupported shape   */
+  PKV_ERR_ALIGN = 2,      /* a pointer misses its required alignment       */
+  PKV_ERR_BAD_PAGE = 3,   /* pkv_status_from_device_error: bad page entry  */
+  PKV_ERR_WORKSPACE = 4,  /* workspace missing or smaller than required    */
+  PKV_ERR_CUDA = 5,       /* a CUDA runtime call failed (launch, query)    */
+  PKV_ERR_DEVICE = 6,     /* current device is not a supported sm_103 GPU  */
+  PKV_ERR_BAD_INPUT = 7   /* pkv_status_from_device_error: other device err */
+} pkv_status;
+
+/* Bits OR-ed into *dev_err by the kernels. */
+#define PKV_DEV_ERR_BAD_PAGE   0x1  /* page entry not in [0, num_pages)          */
+#define PKV_DEV_ERR_BAD_SLOT   0x2  /* batch_idx not in [0, max_batch)           */
+#define PKV_DEV_ERR_BAD_POS    0x4  /* position/seq_len < 0 or past max_blocks   */
+#define PKV_DEV_ERR_LAYOUT     0x8  /* prefill packing precondition violated     */
+#define PKV_DEV_ERR_TIMEOUT    0x10 /* a bounded wait inside a kernel gave up    */
+
+/* Geometry of one layer's paged cache. */
+typedef struct {
+  int num_pages;     /* P: physical pages per pool (page 0 reserved)          */
+  int page_size;     /* ps: token slots per page, multiple of 16               */
+  int num_kv_heads;  /* H_kv                                                   */
+  int head_dim;      /* D, must be 128                                         */
+  int max_batch;     /* rows of page_table (slot 0 reserved)                   */
+  int max_blocks;    /* columns of page_table: logical blocks per sequence     */
+} pkv_cache_desc;
+
+/*
+ * pkv_append - KV append through the page table.
+ * Source: "qwen3_flex_inference.py", attention forward ("Write to paged KV
+ * cache"), capture_decode_cudagraph (the k_cache[addr] = k_val write); the
+ * crash on an unreserved entry: "flex_paged_attention.py" commit log, "Files".
+ *
+ * For each token i in [0, n_tokens) with slot b = batch_idx[i] and position
+ * p = input_pos[i], copies the bytes of k_new[i] and v_new[i] (each bf16
+ * [H_kv, D], contiguous rows of a [n_tokens, H_kv, D] tensor) to pool row
+ *     page_table[b, p / ps] * ps + p % ps
+ * of k_pool and v_pool. Bit-exact byte copy. Tokens with b == 0 (padding
+ * slot) are skipped without error. A token whose slot, block or page entry is
+ * out of range is skipped and sets PKV_DEV_ERR_BAD_SLOT / _BAD_POS / _BAD_PAGE.
+ * Two tokens that address the same row race (the last writer is unspecified).
+ * Decode passes n_tokens = B (one new token per row), prefill passes the
+ * packed tokens.
+ */
+pkv_status pkv_append(const pkv_cache_desc* cache, void* k_pool, void* v_pool,
+                      const int32_t* page_table, const void* k_new,
+                      const void* v_new, const int32_t* batch_idx,
+                      const int32_t* input_pos, int n_tokens, int32_t* dev_err,
+                      cudaStream_t stream);
+
+/*
+ * pkv_decode_workspace_size - bytes of workspace pkv_decode_attention needs
+ * on the CURRENT device for `batch` rows and `num_q_heads` query heads.
+ * max_seq_len is accepted for interface stability; the split-KV schedule
+ * balances work over the device's SMs and its scratch does not grow with
+ * sequence length. Returns 0 for invalid arguments.
+ */
+size_t pkv_decode_workspace_size(const pkv_cache_desc* cache, int batch,
+                                 int num_q_heads, int max_seq_len);
+
+/*
+ * pkv_decode_attention - split-KV GQA decode over the paged cache.
+ * Source: "qwen3_flex_inference.py", _decode_block_mask (causal_offset:
+ * keys kv_idx <= input_pos of the row's own slot), attention forward
+ * (enable_gqa); zero-safe padded rows: "flex_vs_vllm.md", "What broke
+ * correctness and had to be dropped" (ROWS_GUARANTEED_SAFE).
+ *
+ * Row b in [0, batch) has one query token q[b] (bf16 [num_q_heads, D] within
+ * a contiguous [batch, num_q_heads, D] tensor) and attends the first
+ * n = seq_lens[b] logical keys of slot c = batch_idx[b] (for a decode step
+ * seq_lens[b] = input_pos[b] + 1, the new token included). Query head h reads
+ * kv head h / (num_q_heads / num_kv_heads). Writes
+ *   lse[b, h] = ln sum_{t<n} exp(scale * q[b,h] . K[c,t,kvh])       (fp32)
+ *   out[b, h] = sum_{t<n} exp(scale * q[b,h] . K[c,t,kvh] - lse) V[c,t,kvh]
+ * out: bf16 [batch, num_q_heads, D] (rounded to nearest even); lse: fp32
+ * [batch, num_q_heads], natural log. Rows with c == 0 or n == 0 give out = 0
+ * and lse = -inf (never NaN). A row with c outside [0, max_batch) or
+ * n > max_blocks * page_size (or n < 0) sets a PKV_DEV_ERR bit and gives
+ * 0 / -inf; a page entry out of range within the first n keys sets
+ * PKV_DEV_ERR_BAD_PAGE and leaves that row unspecified.
+ *
+ * workspace: device scratch of at least pkv_decode_workspace_size() bytes,
+ * 256-byte aligned, owned by the caller; its contents need no initialisation
+ * and are overwritten; calls that share a workspace must be stream-ordered.
+ * Two kernels run: the split-KV pass and the LSE merge.
+ */
+pkv_status pkv_decode_attention(const pkv_cache_desc* cache, const void* k_pool,
+                                const void* v_pool, const int32_t* page_table,
+                                const void* q, int num_q_heads,
+                                const int32_t* batch_idx,
+                                const int32_t* seq_lens, int batch, float scale,
+                                void* out, float* lse, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_err,
+                                cudaStream_t stream);
+
+/*
+ * pkv_prefill_attention - packed document-causal prefill on tcgen05 tensor
+ * cores. Source: "qwen3_flex_inference.py", _prefill (prompts concatenated
+ * into one sequence with a document-causal mask; the mask built without
+ * paging, so attention reads the packed fresh k/v).
+ *
+ * q: bf16 [n_tokens, num_q_heads, D]; k, v: bf16 [n_tokens, num_kv_heads, D];
+ * batch_idx, input_pos: int32 [n_tokens]. Token i may attend token j iff
+ * batch_idx[j] == batch_idx[i] != 0 and input_pos[j] <= input_pos[i].
+ * Precondition (the pages' packing): each document's tokens are contiguous
+ * and numbered input_pos = 0, 1, 2, ...; padding tokens carry batch_idx 0.
+ * A token that breaks it sets PKV_DEV_ERR_LAYOUT (its row is unspecified).
+ * Writes out bf16 [n_tokens, num_q_heads, D] and lse fp32
+ * [n_tokens, num_q_heads] with the same formulas as decode; padding tokens
+ * give 0 / -inf. Writing the k/v into the pages is a separate pkv_append.
+ */
+pkv_status pkv_prefill_attention(const void* q, const void* k, const void* v,
+                                 int num_q_heads, int num_kv_heads,
+                                 int head_dim, const int32_t* batch_idx,
+                                 const int32_t* input_pos, int n_tokens,
+                                 float scale, void* out, float* lse,
+                                 int32_t* dev_err, cudaStream_t stream);
+
+/* Static, human-readable name of a status. */
+const char* pkv_status_string(pkv_status status);
+
+/* Text of the CUDA runtime error behind the calling thread's most recent
+ * PKV_ERR_CUDA (static storage; "no error" if there was none). */
+const char* pkv_last_cuda_error_string(void);
+
+/* Maps a dev_err word read back by the caller to a status: PKV_OK when 0,
+ * PKV_ERR_BAD_PAGE when the bad-page bit is set, PKV_ERR_BAD_INPUT else. */
+pkv_status pkv_status_from_device_error(int32_t dev_err_value);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,206 @@
+"""Thin ctypes binding over libpkv.so (C ABI in include/pkv.h).
+
+Argument marshalling only: shapes are read from the tensors, outputs are
+allocated with PyTorch when the caller passes none, and every computation
+runs in the library's CUDA kernels on the caller's current stream. There is
+no fallback: if ``libpkv.so`` is missing or fails to load, every call raises.
+
+Functions keep the names of the C entry points:
+``pkv_append``, ``pkv_decode_attention``, ``pkv_decode_workspace_size``,
+``pkv_prefill_attention``, ``pkv_status_string``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpkv.so")
+
+PKV_OK = 0
+STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_ARG", 2: "PKV_ERR_ALIGN",
+                3: "PKV_ERR_BAD_PAGE", 4: "PKV_ERR_WORKSPACE", 5: "PKV_ERR_CUDA",
+                6: "PKV_ERR_DEVICE", 7: "PKV_ERR_BAD_INPUT"}
+DEV_ERR_BAD_PAGE = 0x1
+DEV_ERR_BAD_SLOT = 0x2
+DEV_ERR_BAD_POS = 0x4
+DEV_ERR_LAYOUT = 0x8
+DEV_ERR_TIMEOUT = 0x10
+
+EXPORTED = ("pkv_append", "pkv_decode_workspace_size", "pkv_decode_attention",
+            "pkv_prefill_attention", "pkv_status_string",
+            "pkv_status_from_device_error", "pkv_last_cuda_error_string")
+
+
+class PkvError(RuntimeError):
+    """A libpkv call returned a status other than PKV_OK."""
+
+    def __init__(self, func: str, status: int):
+        self.status = status
+        detail = status_string(status)
+        if status == 5:
+            detail += ": " + load_library().pkv_last_cuda_error_string().decode()
+        super().__init__(f"{func}: {STATUS_NAMES.get(status, status)} ({detail})")
+
+
+class CacheDesc(ctypes.Structure):
+    _fields_ = [("num_pages", ctypes.c_int), ("page_size", ctypes.c_int),
+                ("num_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("max_batch", ctypes.c_int), ("max_blocks", ctypes.c_int)]
+
+
+_lib = None
+
+
+def load_library() -> ctypes.CDLL:
+    """Loads the in-tree libpkv.so (built by ``paged_kv_gqa_pkv_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -m paged_kv_gqa_pkv_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32p, f32p = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+    c_int, c_float, c_size = ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    desc_p = ctypes.POINTER(CacheDesc)
+    lib.pkv_append.argtypes = [desc_p, vp, vp, i32p, vp, vp, i32p, i32p, c_int, i32p, vp]
+    lib.pkv_append.restype = c_int
+    lib.pkv_decode_workspace_size.argtypes = [desc_p, c_int, c_int, c_int]
+    lib.pkv_decode_workspace_size.restype = c_size
+    lib.pkv_decode_attention.argtypes = [desc_p, vp, vp, i32p, vp, c_int, i32p, i32p, c_int,
+                                         c_float, vp, f32p, vp, c_size, i32p, vp]
+    lib.pkv_decode_attention.restype = c_int
+    lib.pkv_prefill_attention.argtypes = [vp, vp, vp, c_int, c_int, c_int, i32p, i32p, c_int,
+                                          c_float, vp, f32p, i32p, vp]
+    lib.pkv_prefill_attention.restype = c_int
+    lib.pkv_status_string.argtypes = [c_int]
+    lib.pkv_status_string.restype = ctypes.c_char_p
+    lib.pkv_last_cuda_error_string.argtypes = []
+    lib.pkv_last_cuda_error_string.restype = ctypes.c_char_p
+    lib.pkv_status_from_device_error.argtypes = [ctypes.c_int32]
+    lib.pkv_status_from_device_error.restype = c_int
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().pkv_status_string(int(status)).decode()
+
+
+pkv_status_string = status_string
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype or t.dim() != ndim or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor of rank {ndim}, "
+                         f"got {t.dtype} {tuple(t.shape)} on {t.device}")
+
+
+def cache_desc(k_pool: torch.Tensor, page_table: torch.Tensor, page_size: int) -> CacheDesc:
+    rows, hkv, d = k_pool.shape
+    if rows % page_size:
+        raise ValueError("pool rows must be a multiple of page_size")
+    return CacheDesc(rows // page_size, page_size, hkv, d, page_table.shape[0],
+                     page_table.shape[1])
+
+
+def _check(func: str, status: int):
+    if status != PKV_OK:
+        raise PkvError(func, status)
+
+
+def pkv_append(k_pool, v_pool, page_table, k_new, v_new, batch_idx, input_pos,
+               page_size: int, dev_err=None, stream=None) -> None:
+    """Writes k_new/v_new [N, H_kv, D] into the pools through the page table."""
+    for name, t, dt, nd in (("k_pool", k_pool, torch.bfloat16, 3),
+                            ("v_pool", v_pool, torch.bfloat16, 3),
+                            ("page_table", page_table, torch.int32, 2),
+                            ("k_new", k_new, torch.bfloat16, 3),
+                            ("v_new", v_new, torch.bfloat16, 3),
+                            ("batch_idx", batch_idx, torch.int32, 1),
+                            ("input_pos", input_pos, torch.int32, 1)):
+        _need(t, name, dt, nd)
+    desc = cache_desc(k_pool, page_table, page_size)
+    st = load_library().pkv_append(
+        ctypes.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(k_new),
+        _ptr(v_new), _ptr(batch_idx), _ptr(input_pos), int(batch_idx.numel()),
+        _ptr(dev_err), _stream(stream))
+    _check("pkv_append", st)
+
+
+def pkv_decode_workspace_size(k_pool, page_table, page_size: int, batch: int,
+                              num_q_heads: int, max_seq_len: int = 0) -> int:
+    desc = cache_desc(k_pool, page_table, page_size)
+    n = load_library().pkv_decode_workspace_size(ctypes.byref(desc), batch, num_q_heads,
+                                                 max_seq_len)
+    if n == 0 and batch > 0:
+        raise PkvError("pkv_decode_workspace_size", 1)
+    return int(n)
+
+
+def pkv_decode_attention(k_pool, v_pool, page_table, q, batch_idx, seq_lens,
+                         page_size: int, scale: float, out=None, lse=None,
+                         workspace=None, dev_err=None, stream=None):
+    """Split-KV GQA decode. q [B, Hq, D] bf16 -> (out [B, Hq, D] bf16,
+    lse [B, Hq] fp32)."""
+    _need(q, "q", torch.bfloat16, 3)
+    for name, t, dt, nd in (("k_pool", k_pool, torch.bfloat16, 3),
+                            ("v_pool", v_pool, torch.bfloat16, 3),
+                            ("page_table", page_table, torch.int32, 2),
+                            ("batch_idx", batch_idx, torch.int32, 1),
+                            ("seq_lens", seq_lens, torch.int32, 1)):
+        _need(t, name, dt, nd)
+    B, hq, d = q.shape
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, hq), dtype=torch.float32, device=q.device)
+    desc = cache_desc(k_pool, page_table, page_size)
+    lib = load_library()
+    if workspace is None:
+        n = lib.pkv_decode_workspace_size(ctypes.byref(desc), B, hq, 0)
+        workspace = torch.empty(max(int(n), 256), dtype=torch.uint8, device=q.device)
+    st = lib.pkv_decode_attention(
+        ctypes.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(q), hq,
+        _ptr(batch_idx), _ptr(seq_lens), B, float(scale), _ptr(out), _ptr(lse),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_err),
+        _stream(stream))
+    _check("pkv_decode_attention", st)
+    return out, lse
+
+
+def pkv_prefill_attention(q, k, v, batch_idx, input_pos, scale: float, out=None,
+                          lse=None, dev_err=None, stream=None):
+    """Packed document-causal prefill. q [T, Hq, D], k/v [T, H_kv, D] bf16 ->
+    (out [T, Hq, D] bf16, lse [T, Hq] fp32)."""
+    for name, t, dt, nd in (("q", q, torch.bfloat16, 3), ("k", k, torch.bfloat16, 3),
+                            ("v", v, torch.bfloat16, 3),
+                            ("batch_idx", batch_idx, torch.int32, 1),
+                            ("input_pos", input_pos, torch.int32, 1)):
+        _need(t, name, dt, nd)
+    T, hq, d = q.shape
+    if out is None:
+        out = torch.empty((T, hq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, hq), dtype=torch.float32, device=q.device)
+    st = load_library().pkv_prefill_attention(
+        _ptr(q), _ptr(k), _ptr(v), hq, k.shape[1], d, _ptr(batch_idx), _ptr(input_pos), T,
+        float(scale), _ptr(out), _ptr(lse), _ptr(dev_err), _stream(stream))
+    _check("pkv_prefill_attention", st)
+    return out, lse

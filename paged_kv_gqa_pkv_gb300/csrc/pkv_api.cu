@@ -1,0 +1,256 @@
+// pkv_api.cu - the extern "C" entry points of libpkv (declared in pkv.h):
+// synchronous host validation, TMA descriptor encoding and kernel launches.
+// Nothing here allocates device memory or synchronises a stream.
+#include <climits>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <utility>
+
+#include "pkv.h"
+#include "pkv_launch.h"
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver, found through the runtime so the
+// library does not link against libcuda.
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+struct DeviceInfo {
+  bool known = false;
+  bool supported = false;
+  int sm_count = 0;
+};
+
+constexpr int kMaxDevices = 64;
+
+// SM count and architecture of `dev`, queried once per device.
+pkv_status device_info(int* sm_count) {
+  static DeviceInfo cache[kMaxDevices];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(mu);
+  DeviceInfo& d = cache[dev];
+  if (!d.known) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    d.supported = (major == 10 && minor == 3);  // built for sm_103a only
+    d.sm_count = sms;
+    d.known = true;
+  }
+  if (!d.supported) return PKV_ERR_DEVICE;
+  *sm_count = d.sm_count;
+  return PKV_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+// Records a failed runtime call for pkv_last_cuda_error_string().
+pkv_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return PKV_OK;
+  t_last_cuda_error = e;
+  return PKV_ERR_CUDA;
+}
+
+pkv_status check_cache(const pkv_cache_desc* c) {
+  if (c == nullptr) return PKV_ERR_ARG;
+  if (c->num_pages <= 0 || c->page_size <= 0 || c->page_size % 16 != 0) return PKV_ERR_ARG;
+  if (c->num_kv_heads <= 0 || c->head_dim != pkv::kHeadDim) return PKV_ERR_ARG;
+  if (c->max_batch <= 0 || c->max_blocks <= 0) return PKV_ERR_ARG;
+  if (static_cast<long long>(c->num_pages) * c->page_size > INT_MAX) return PKV_ERR_ARG;
+  if (static_cast<long long>(c->max_blocks) * c->page_size > INT_MAX) return PKV_ERR_ARG;
+  if (static_cast<long long>(c->max_batch) * c->max_blocks > INT_MAX) return PKV_ERR_ARG;
+  return PKV_OK;
+}
+
+bool group_ok(int num_q_heads, int num_kv_heads) {
+  if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return false;
+  const int g = num_q_heads / num_kv_heads;
+  return g == 1 || g == 2 || g == 4 || g == 8;
+}
+
+// 3-D view {D, H_kv, rows} of a token-major pool; a box is 16 rows of one head.
+pkv_status encode_pool_map(CUtensorMap* map, const void* pool, const pkv_cache_desc* c) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr) return PKV_ERR_CUDA;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(c->head_dim),
+                              static_cast<cuuint64_t>(c->num_kv_heads),
+                              static_cast<cuuint64_t>(c->num_pages) * c->page_size};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(c->head_dim) * 2,
+                                 static_cast<cuuint64_t>(c->num_kv_heads) * c->head_dim * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(c->head_dim), 1u,
+                             static_cast<cuuint32_t>(pkv::kDecodeTile)};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  std::memset(map, 0, sizeof(*map));
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_ARG;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_ARG: return "invalid argument";
+    case PKV_ERR_ALIGN: return "misaligned pointer";
+    case PKV_ERR_BAD_PAGE: return "page table entry out of range";
+    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKV_ERR_CUDA: return "CUDA runtime error";
+    case PKV_ERR_DEVICE: return "current device is not a supported sm_103 GPU";
+    case PKV_ERR_BAD_INPUT: return "invalid slot, position or packing found on the device";
+  }
+  return "unknown status";
+}
+
+const char* pkv_last_cuda_error_string(void) {
+  return t_last_cuda_error == cudaSuccess ? "no error" : cudaGetErrorString(t_last_cuda_error);
+}
+
+pkv_status pkv_status_from_device_error(int32_t v) {
+  if (v == 0) return PKV_OK;
+  if (v & PKV_DEV_ERR_BAD_PAGE) return PKV_ERR_BAD_PAGE;
+  return PKV_ERR_BAD_INPUT;
+}
+
+pkv_status pkv_append(const pkv_cache_desc* cache, void* k_pool, void* v_pool,
+                      const int32_t* page_table, const void* k_new, const void* v_new,
+                      const int32_t* batch_idx, const int32_t* input_pos, int n_tokens,
+                      int32_t* dev_err, cudaStream_t stream) {
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (n_tokens < 0) return PKV_ERR_ARG;
+  if (n_tokens == 0) return PKV_OK;
+  if (!k_pool || !v_pool || !page_table || !k_new || !v_new || !batch_idx || !input_pos)
+    return PKV_ERR_ARG;
+  if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) ||
+      !aligned(page_table, 4) || !aligned(batch_idx, 4) || !aligned(input_pos, 4) ||
+      !aligned(dev_err, 4))
+    return PKV_ERR_ALIGN;
+  int sms = 0;
+  st = device_info(&sms);
+  if (st != PKV_OK) return st;
+  pkv::AppendParams p;
+  p.k_pool = k_pool;
+  p.v_pool = v_pool;
+  p.page_table = page_table;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.batch_idx = batch_idx;
+  p.input_pos = input_pos;
+  p.dev_err = dev_err;
+  p.n_tokens = n_tokens;
+  p.row_vecs = cache->num_kv_heads * cache->head_dim * 2 / 16;
+  p.page_size = cache->page_size;
+  p.num_pages = cache->num_pages;
+  p.max_batch = cache->max_batch;
+  p.max_blocks = cache->max_blocks;
+  return cuda_status(pkv::launch_append(p, stream));
+}
+
+size_t pkv_decode_workspace_size(const pkv_cache_desc* cache, int batch, int num_q_heads,
+                                 int max_seq_len) {
+  (void)max_seq_len;
+  if (check_cache(cache) != PKV_OK || batch < 0 || batch > pkv::kDecodeMaxBatch) return 0;
+  if (!group_ok(num_q_heads, cache->num_kv_heads)) return 0;
+  int sms = 0;
+  if (device_info(&sms) != PKV_OK) return 0;
+  return pkv::decode_workspace_bytes(batch, cache->num_kv_heads,
+                                     num_q_heads / cache->num_kv_heads,
+                                     pkv::decode_workers_for_device(sms));
+}
+
+pkv_status pkv_decode_attention(const pkv_cache_desc* cache, const void* k_pool,
+                                const void* v_pool, const int32_t* page_table, const void* q,
+                                int num_q_heads, const int32_t* batch_idx,
+                                const int32_t* seq_lens, int batch, float scale, void* out,
+                                float* lse, void* workspace, size_t workspace_bytes,
+                                int32_t* dev_err, cudaStream_t stream) {
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (batch < 0 || batch > pkv::kDecodeMaxBatch) return PKV_ERR_ARG;
+  if (!group_ok(num_q_heads, cache->num_kv_heads)) return PKV_ERR_ARG;
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return PKV_ERR_ARG;
+  if (batch == 0) return PKV_OK;
+  if (!k_pool || !v_pool || !page_table || !q || !batch_idx || !seq_lens || !out || !lse)
+    return PKV_ERR_ARG;
+  if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(q, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4) || !aligned(page_table, 4) || !aligned(batch_idx, 4) ||
+      !aligned(seq_lens, 4) || !aligned(dev_err, 4))
+    return PKV_ERR_ALIGN;
+  int sms = 0;
+  st = device_info(&sms);
+  if (st != PKV_OK) return st;
+  const int group = num_q_heads / cache->num_kv_heads;
+  const int workers = pkv::decode_workers_for_device(sms);
+  const size_t need = pkv::decode_workspace_bytes(batch, cache->num_kv_heads, group, workers);
+  if (workspace == nullptr || workspace_bytes < need) return PKV_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return PKV_ERR_ALIGN;
+
+  CUtensorMap kmap, vmap;
+  st = encode_pool_map(&kmap, k_pool, cache);
+  if (st != PKV_OK) return st;
+  st = encode_pool_map(&vmap, v_pool, cache);
+  if (st != PKV_OK) return st;
+
+  const size_t slots = static_cast<size_t>(workers) + static_cast<size_t>(batch) * cache->num_kv_heads;
+  const size_t part_bytes = slots * pkv::decode_slot_floats(group) * sizeof(float);
+  pkv::DecodeParams p;
+  p.q = q;
+  p.page_table = page_table;
+  p.batch_idx = batch_idx;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.lse = lse;
+  p.partials = static_cast<float*>(workspace);
+  p.prefix = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + ((part_bytes + 255) / 256) * 256);
+  p.dev_err = dev_err;
+  p.batch = batch;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = cache->num_kv_heads;
+  p.page_size = cache->page_size;
+  p.num_pages = cache->num_pages;
+  p.max_batch = cache->max_batch;
+  p.max_blocks = cache->max_blocks;
+  p.num_workers = workers;
+  p.qscale = scale * 1.4426950408889634f;
+  return cuda_status(pkv::launch_decode(p, kmap, vmap, sms, stream));
+}
+
+pkv_status pkv_prefill_attention(const void* q, const void* k, const void* v, int num_q_heads,
+                                 int num_kv_heads, int head_dim, const int32_t* batch_idx,
+                                 const int32_t* input_pos, int n_tokens, float scale, void* out,
+                                 float* lse, int32_t* dev_err, cudaStream_t stream) {
+  return pkv::prefill_entry(q, k, v, num_q_heads, num_kv_heads, head_dim, batch_idx, input_pos,
+                            n_tokens, scale, out, lse, dev_err, stream);
+}
+
+}  // extern "C"

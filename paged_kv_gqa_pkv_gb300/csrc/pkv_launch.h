@@ -1,0 +1,97 @@
+// pkv_launch.h - parameter blocks and launch entry points of the libpkv
+// kernels (internal; the public ABI is include/pkv.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <utility>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "pkv_device.cuh"
+
+namespace pkv {
+
+struct AppendParams {
+  void* k_pool;
+  void* v_pool;
+  const int32_t* page_table;
+  const void* k_new;
+  const void* v_new;
+  const int32_t* batch_idx;
+  const int32_t* input_pos;
+  int32_t* dev_err;
+  int n_tokens;
+  int row_vecs;     // 16-byte vectors per token row = H_kv * D * 2 / 16
+  int page_size;
+  int num_pages;
+  int max_batch;
+  int max_blocks;
+};
+
+// Split-KV decode. The work of a call is the sequence of 16-token tiles of all
+// (row, kv head) items, rows in order, kv heads within a row; it is cut into
+// num_workers equal contiguous ranges, one per warp of a persistent grid.
+struct DecodeParams {
+  const void* q;              // bf16 [B, Hq, D]
+  const int32_t* page_table;  // [max_batch, max_blocks]
+  const int32_t* batch_idx;   // [B]
+  const int32_t* seq_lens;    // [B]
+  void* out;                  // bf16 [B, Hq, D]
+  float* lse;                 // [B, Hq]
+  float* partials;            // workspace: (num_workers + B*Hkv) slots
+  int32_t* prefix;            // workspace: [B + 1] tile prefix over rows
+  int32_t* dev_err;
+  int batch;
+  int num_q_heads;
+  int num_kv_heads;
+  int page_size;
+  int num_pages;
+  int max_batch;
+  int max_blocks;
+  int num_workers;
+  float qscale;               // scale * log2(e): scores kept in log2 units
+};
+
+constexpr int kDecodeTile = 16;       // tokens per pipeline stage
+constexpr int kDecodeWarps = 8;       // workers (warps) per CTA
+constexpr int kDecodeStages = 3;      // stages in flight per worker
+constexpr int kDecodeMaxBatch = 1024; // rows per call (prefix lives in smem)
+
+// Floats per partial slot: unnormalised o[G][D], then m[G], l[G] (padded).
+__host__ __device__ constexpr int decode_slot_floats(int g) {
+  return g * kHeadDim + ((2 * g + 3) / 4) * 4;
+}
+
+size_t decode_workspace_bytes(int batch, int num_kv_heads, int group, int num_workers);
+int decode_workers_for_device(int sm_count);
+
+cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+
+// Validation and launch of pkv_prefill_attention (pkv_prefill.cu).
+pkv_status prefill_entry(const void* q, const void* k, const void* v, int num_q_heads,
+                         int num_kv_heads, int head_dim, const int32_t* batch_idx,
+                         const int32_t* input_pos, int n_tokens, float scale, void* out,
+                         float* lse, int32_t* dev_err, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          int sm_count, cudaStream_t stream);
+
+// cudaLaunchKernelEx with an optional programmatic-stream-serialisation
+// attribute (programmatic dependent launch).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, bool programmatic, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = programmatic ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+}  // namespace pkv

@@ -1,0 +1,158 @@
+"""K2/K3 split-KV decode on the GPU against the float64 oracle, on the four
+decode workloads at full size and on edge cases (tile edges, empty rows,
+padding rows, NaN garbage in unused slots, bad entries, other GQA groups,
+changing batch sizes in one process)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.paged_attention as orc
+from paged_kv_gqa_pkv_gb300 import binding
+from paged_kv_gqa_pkv_gb300 import workloads as W
+from paged_kv_gqa_pkv_gb300.workloads import bf16_bits
+from tests.parity import (assert_attention_close, gpu, new_dev_err, oracle_decode_step,
+                          run_decode_step)
+
+pytestmark = pytest.mark.gpu
+
+
+def _full_parity(case):
+    kp, vp, out, lse, err = run_decode_step(case)
+    ek, ev, ref_o, ref_l, bad_tok, bad_rows = oracle_decode_step(case)
+    assert err == 0 and not bad_tok and not bad_rows
+    assert np.array_equal(bf16_bits(kp), ek) and np.array_equal(bf16_bits(vp), ev)
+    return assert_attention_close(out, lse, ref_o, ref_l, tag=case.name)
+
+
+def test_tiny_decode():
+    _full_parity(W.tiny_decode(0))
+
+
+@pytest.mark.parametrize("permute", [False, True], ids=["sequential", "permuted"])
+def test_qwen3_b64_decode(permute):
+    _full_parity(W.qwen3_b64_decode(0, permute=permute))
+
+
+def test_padded_bucket_decode():
+    c = W.padded_bucket_decode(0)
+    _, _, out, lse, err = run_decode_step(c)
+    assert err == 0
+    assert torch.all(out[40:] == 0) and torch.all(torch.isneginf(lse[40:]))
+    _full_parity(c)
+
+
+def test_long_context_b256_decode():
+    _full_parity(W.long_context_decode(0))
+
+
+def _permute_pages(case, seed):
+    """Same logical content, pages moved by a random permutation."""
+    P, ps = case.num_pages, case.page_size
+    rng = np.random.default_rng(seed)
+    sigma = np.concatenate([[0], rng.permutation(np.arange(1, P))])
+    kp = torch.empty_like(case.k_pool)
+    vp = torch.empty_like(case.v_pool)
+    for p in range(P):
+        kp[sigma[p] * ps:(sigma[p] + 1) * ps] = case.k_pool[p * ps:(p + 1) * ps]
+        vp[sigma[p] * ps:(sigma[p] + 1) * ps] = case.v_pool[p * ps:(p + 1) * ps]
+    t = case.page_table.numpy()
+    t2 = np.where(t >= 0, sigma[np.maximum(t, 0)], -1).astype(np.int32)
+    import copy
+    c2 = copy.copy(case)
+    c2.k_pool, c2.v_pool, c2.page_table = kp, vp, torch.from_numpy(t2)
+    return c2
+
+
+def test_contiguous_fast_path_bitwise_equals_general_path():
+    seq = W.qwen3_b64_decode(0, permute=False)
+    perm = _permute_pages(seq, 1)
+    _, _, o1, l1, e1 = run_decode_step(seq)
+    _, _, o2, l2, e2 = run_decode_step(perm)
+    assert e1 == 0 and e2 == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 8), (32, 4), (8, 2)])
+def test_other_gqa_groups(hq, hkv):
+    lens = [1, 15, 16, 17, 31, 32, 33, 100, 0, 257]
+    c = W.custom_decode(5, lens, hq=hq, hkv=hkv, page_size=32, permute=True)
+    # a live row with no keys has no position to append to: attend only
+    kp, vp, out, lse, err = run_decode_step(c, append=False)
+    _, _, ref_o, ref_l, _, bad_rows = oracle_decode_step(c, append=False)
+    assert err == 0 and not bad_rows
+    assert_attention_close(out, lse, ref_o, ref_l, tag=f"G={hq // hkv}")
+    assert torch.all(out[8] == 0) and torch.all(torch.isneginf(lse[8]))
+
+
+def test_single_key_returns_its_value_row():
+    c = W.custom_decode(7, [1, 1, 1], hq=32, hkv=8, page_size=128)
+    kp, vp, out, lse, err = run_decode_step(c)
+    g = 4
+    for b in range(3):
+        for h in range(32):
+            assert torch.equal(out[b, h], c.v_new[b, h // g])
+
+
+def test_unused_slots_hold_nan_garbage():
+    """Slots past each sequence's length (inside its last page) hold NaN; the
+    kernel must never let them into a result."""
+    c = W.custom_decode(9, [5, 17, 130, 40], hq=32, hkv=8, page_size=128, fill=float("nan"))
+    gen = torch.Generator().manual_seed(2)
+    for s, n in enumerate(c.seq_lens.tolist(), start=1):
+        for t in range(n):
+            row = int(c.page_table[s, t // 128]) * 128 + t % 128
+            c.k_pool[row] = torch.randn((8, 128), generator=gen).to(torch.bfloat16)
+            c.v_pool[row] = torch.randn((8, 128), generator=gen).to(torch.bfloat16)
+    _full_parity(c)
+
+
+def test_bad_page_entry_flagged_other_rows_exact():
+    c = W.custom_decode(11, [40, 300, 90], hq=32, hkv=8, page_size=128, permute=True)
+    c.page_table[2, 1] = -1
+    kp, vp, out, lse, err = run_decode_step(c, append=False)
+    assert err & binding.DEV_ERR_BAD_PAGE
+    _, _, ref_o, ref_l, _, bad_rows = oracle_decode_step(c, append=False)
+    assert bad_rows == [1]
+    assert_attention_close(out, lse, ref_o, ref_l, rows=[0, 2])
+
+
+def test_bad_slot_and_overlong_rows_give_zero():
+    c = W.custom_decode(13, [40, 70, 90], hq=32, hkv=8, page_size=128, permute=True)
+    c.batch_idx[0] = 77                      # slot past the table
+    c.seq_lens[1] = c.max_blocks * 128 + 1   # longer than the table allows
+    _, _, out, lse, err = run_decode_step(c, append=False)
+    assert err & binding.DEV_ERR_BAD_SLOT and err & binding.DEV_ERR_BAD_POS
+    assert torch.all(out[:2] == 0) and torch.all(torch.isneginf(lse[:2]))
+    _, _, ref_o, ref_l, _, _ = oracle_decode_step(c, append=False, rows=[2])
+    assert_attention_close(out, lse, ref_o, ref_l, rows=[2])
+
+
+def test_changing_batch_sizes_in_one_process():
+    """One library, many shapes: no per-shape state may leak between calls."""
+    for B in (1, 64, 3, 200, 2):
+        lens = torch.randint(1, 700, (B,), generator=torch.Generator().manual_seed(B)).tolist()
+        c = W.custom_decode(B, lens, hq=32, hkv=8, page_size=128, permute=True)
+        _full_parity(c)
+
+
+def test_decode_rejects_bad_host_arguments():
+    c = W.tiny_decode(0)
+    kp, vp, table = gpu(c.k_pool), gpu(c.v_pool), gpu(c.page_table)
+    q, bidx, lens = gpu(c.q), gpu(c.batch_idx), gpu(c.seq_lens)
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(binding.PkvError) as e:
+        binding.pkv_decode_attention(kp, vp, table, q, bidx, lens, c.page_size, c.scale,
+                                     workspace=small)
+    assert e.value.status == 4
+    with pytest.raises(binding.PkvError) as e:   # page size not a multiple of 16
+        binding.pkv_decode_attention(kp, vp, table, q, bidx, lens, 8, c.scale)
+    assert e.value.status == 1
+    q_off = torch.empty(q.numel() + 4, dtype=torch.bfloat16, device="cuda")[4:].view(q.shape)
+    with pytest.raises(binding.PkvError) as e:   # 16-byte misaligned q
+        binding.pkv_decode_attention(kp, vp, table, q_off, bidx, lens, c.page_size, c.scale)
+    assert e.value.status == 2
+    q6 = torch.zeros((4, 6, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(binding.PkvError) as e:   # group 3 unsupported
+        binding.pkv_decode_attention(kp, vp, table, q6, bidx, lens, c.page_size, c.scale)
+    assert e.value.status == 1
