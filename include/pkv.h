@@ -157,7 +157,8 @@ pkv_status pkv_decode_attention(const pkv_cache_desc* cache, const void* k_pool,
  * A token that breaks it sets PKV_DEV_ERR_LAYOUT (its row is unspecified).
  * Writes out bf16 [n_tokens, num_q_heads, D] and lse fp32
  * [n_tokens, num_q_heads] with the same formulas as decode; padding tokens
- * give 0 / -inf. Writing the k/v into the pages is a separate pkv_append.
+ * give 0 / -inf. scale must be finite and > 0. Writing the k/v into the
+ * pages is a separate pkv_append.
  */
 pkv_status pkv_prefill_attention(const void* q, const void* k, const void* v,
                                  int num_q_heads, int num_kv_heads,

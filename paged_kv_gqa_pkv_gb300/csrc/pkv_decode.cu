@@ -442,60 +442,77 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
   }
 }
 
+// One warp per (row, q head): lanes load the segments' (m, l) in parallel,
+// the o loads of the first segments go out in the same round, and the LSE
+// combination is a warp reduction.
 template <int G>
 __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p) {
   pdl_wait_primary();
   const int lane = threadIdx.x & 31;
-  const int item = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int wid = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (wid >= p.batch * p.num_q_heads) return;
+  const int b = wid / p.num_q_heads;
+  const int h = wid % p.num_q_heads;
+  const int kvh = h / G;
+  const int g = h % G;
   const int hkv = p.num_kv_heads;
-  if (item >= p.batch * hkv) return;
-  const int b = item / hkv;
-  const int kvh = item % hkv;
   const int pb = p.prefix[b];
   const int tiles = p.prefix[b + 1] - pb;
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) +
-                       (static_cast<int64_t>(b) * p.num_q_heads + kvh * G) * kHeadDim + lane * 4;
-  float* lse = p.lse + static_cast<int64_t>(b) * p.num_q_heads + kvh * G;
+  const int64_t total = static_cast<int64_t>(p.prefix[p.batch]) * hkv;
+  __nv_bfloat16* out =
+      static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(wid) * kHeadDim + lane * 4;
   if (tiles == 0) {
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-      *reinterpret_cast<uint2*>(out + g * kHeadDim) = make_uint2(0u, 0u);
-    if (lane < G) lse[lane] = -INFINITY;
+    *reinterpret_cast<uint2*>(out) = make_uint2(0u, 0u);
+    if (lane == 0) p.lse[wid] = -INFINITY;
     return;
   }
-  const int64_t total = static_cast<int64_t>(p.prefix[p.batch]) * hkv;
   const int64_t per = (total + p.num_workers - 1) / p.num_workers;
   const int64_t u0 = static_cast<int64_t>(pb) * hkv + static_cast<int64_t>(kvh) * tiles;
   const int w0 = static_cast<int>(u0 / per);
-  const int w1 = static_cast<int>((u0 + tiles - 1) / per);
+  const int nseg = static_cast<int>((u0 + tiles - 1) / per) - w0 + 1;
   constexpr int SF = decode_slot_floats(G);
-  const float* slots = p.partials + (static_cast<int64_t>(w0) + item) * SF;
-  const int nseg = w1 - w0 + 1;
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    float M = -INFINITY;
-    for (int s = 0; s < nseg; ++s) M = fmaxf(M, slots[s * SF + G * kHeadDim + g]);
-    float L = 0.f;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < nseg; ++s) {
-      const float* sl = slots + s * SF;
-      const float sc = exp2f(sl[G * kHeadDim + g] - M);
-      L = fmaf(sl[G * kHeadDim + G + g], sc, L);
-      const float4 ov = *reinterpret_cast<const float4*>(sl + g * kHeadDim + lane * 4);
-      o.x = fmaf(ov.x, sc, o.x);
-      o.y = fmaf(ov.y, sc, o.y);
-      o.z = fmaf(ov.z, sc, o.z);
-      o.w = fmaf(ov.w, sc, o.w);
-    }
-    const float inv = 1.f / L;
-    const __nv_bfloat162 lo = __floats2bfloat162_rn(o.x * inv, o.y * inv);
-    const __nv_bfloat162 hi = __floats2bfloat162_rn(o.z * inv, o.w * inv);
-    uint2 packed;
-    packed.x = *reinterpret_cast<const uint32_t*>(&lo);
-    packed.y = *reinterpret_cast<const uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(out + g * kHeadDim) = packed;
-    if (lane == 0) lse[g] = (M + log2f(L)) * 0.69314718055994531f;
+  const float* slots = p.partials + (static_cast<int64_t>(w0) + static_cast<int64_t>(b) * hkv + kvh) * SF;
+
+  float M = -INFINITY;
+  for (int s0 = 0; s0 < nseg; s0 += 32) {
+    const int s = s0 + lane;
+    if (s < nseg) M = fmaxf(M, slots[static_cast<int64_t>(s) * SF + G * kHeadDim + g]);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < nseg; s0 += 32) {
+    const int s = s0 + lane;
+    float sc = 0.f;
+    if (s < nseg) {
+      const float* sl = slots + static_cast<int64_t>(s) * SF;
+      sc = exp2f(sl[G * kHeadDim + g] - M);
+      L = fmaf(sl[G * kHeadDim + G + g], sc, L);
+    }
+    const int n = min(32, nseg - s0);
+#pragma unroll 4
+    for (int j = 0; j < n; ++j) {
+      const float scj = __shfl_sync(0xffffffffu, sc, j);
+      const float4 ov = *reinterpret_cast<const float4*>(
+          slots + static_cast<int64_t>(s0 + j) * SF + g * kHeadDim + lane * 4);
+      acc.x = fmaf(ov.x, scj, acc.x);
+      acc.y = fmaf(ov.y, scj, acc.y);
+      acc.z = fmaf(ov.z, scj, acc.z);
+      acc.w = fmaf(ov.w, scj, acc.w);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  const float inv = 1.f / L;
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+  uint2 packed;
+  packed.x = *reinterpret_cast<const uint32_t*>(&lo);
+  packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(out) = packed;
+  if (lane == 0) p.lse[wid] = (M + log2f(L)) * 0.69314718055994531f;
 }
 
 size_t decode_workspace_bytes(int batch, int num_kv_heads, int group, int num_workers) {
@@ -529,8 +546,8 @@ static cudaError_t launch_decode_g(const DecodeParams& p, const CUtensorMap& kma
   e = launch_kernel(decode_splitkv_kernel<G>, dim3(sm_count), dim3(kDecodeWarps * 32), smem,
                     stream, /*programmatic=*/true, kmap, vmap, p);
   if (e != cudaSuccess) return e;
-  const int items = p.batch * p.num_kv_heads;
-  return launch_kernel(decode_merge_kernel<G>, dim3((items + 7) / 8), dim3(256), 0, stream,
+  const int rows = p.batch * p.num_q_heads;
+  return launch_kernel(decode_merge_kernel<G>, dim3((rows + 7) / 8), dim3(256), 0, stream,
                        /*programmatic=*/true, p);
 }
 
