@@ -144,6 +144,37 @@ pkv_status pkv_decode_attention(const pkv_cache_desc* cache, const void* k_pool,
                                 cudaStream_t stream);
 
 /*
+ * pkv_decode_attention_static_scratch - pkv_decode_attention for callers that
+ * cannot allocate device memory. The source pages have no counterpart: this
+ * is a deployment convenience of this library.
+ *
+ * Some callers cannot hand pkv_decode_attention a workspace, because they may
+ * not call cudaMalloc at all: code that runs inside a custom allocator's own
+ * hooks, processes whose device memory is reserved entirely at start-up, or
+ * plug-in hosts that forbid allocations once running. This entry point takes
+ * the same arguments minus the workspace and uses a scratch array compiled
+ * into the library instead: a file-scope __device__ array of 8 MiB, held on
+ * every GPU that loads the library until the process exits. It allocates
+ * nothing and calls no allocating routine.
+ *  - A call whose pkv_decode_workspace_size() exceeds 8 MiB returns
+ *    PKV_ERR_WORKSPACE without launching (about 350 rows at 8 KV heads and a
+ *    GQA group of 4 on a 152-SM GB300; use pkv_decode_attention beyond that).
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current and caches it; make that
+ *    first call before any stream capture.
+ *  - All calls share the one array. Its contents from the previous call are
+ *    never read before being overwritten, so nothing needs clearing, but two
+ *    calls whose kernels overlap on the GPU (different streams, or different
+ *    host threads without ordering) race on it: keep them stream-ordered.
+ * Results are those of pkv_decode_attention on the same inputs.
+ */
+pkv_status pkv_decode_attention_static_scratch(
+    const pkv_cache_desc* cache, const void* k_pool, const void* v_pool,
+    const int32_t* page_table, const void* q, int num_q_heads,
+    const int32_t* batch_idx, const int32_t* seq_lens, int batch, float scale,
+    void* out, float* lse, int32_t* dev_err, cudaStream_t stream);
+
+/*
  * pkv_prefill_attention - packed document-causal prefill on tcgen05 tensor
  * cores. Source: "qwen3_flex_inference.py", _prefill (prompts concatenated
  * into one sequence with a document-causal mask; the mask built without

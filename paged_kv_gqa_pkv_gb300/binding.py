@@ -77,6 +77,10 @@ def load_library() -> ctypes.CDLL:
     lib.pkv_prefill_attention.argtypes = [vp, vp, vp, c_int, c_int, c_int, i32p, i32p, c_int,
                                           c_float, vp, f32p, i32p, vp]
     lib.pkv_prefill_attention.restype = c_int
+    lib.pkv_decode_attention_static_scratch.argtypes = [desc_p, vp, vp, i32p, vp, c_int, i32p,
+                                                        i32p, c_int, c_float, vp, f32p, i32p,
+                                                        vp]
+    lib.pkv_decode_attention_static_scratch.restype = c_int
     lib.pkv_status_string.argtypes = [c_int]
     lib.pkv_status_string.restype = ctypes.c_char_p
     lib.pkv_last_cuda_error_string.argtypes = []
@@ -182,6 +186,33 @@ def pkv_decode_attention(k_pool, v_pool, page_table, q, batch_idx, seq_lens,
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_err),
         _stream(stream))
     _check("pkv_decode_attention", st)
+    return out, lse
+
+
+def pkv_decode_attention_static_scratch(k_pool, v_pool, page_table, q, batch_idx, seq_lens,
+                                        page_size: int, scale: float, out=None, lse=None,
+                                        dev_err=None, stream=None):
+    """Decode for callers that cannot allocate device memory: same result as
+    ``pkv_decode_attention``, with the library's built-in 8 MiB scratch array
+    instead of a caller workspace (calls must not overlap on the GPU)."""
+    _need(q, "q", torch.bfloat16, 3)
+    for name, t, dt, nd in (("k_pool", k_pool, torch.bfloat16, 3),
+                            ("v_pool", v_pool, torch.bfloat16, 3),
+                            ("page_table", page_table, torch.int32, 2),
+                            ("batch_idx", batch_idx, torch.int32, 1),
+                            ("seq_lens", seq_lens, torch.int32, 1)):
+        _need(t, name, dt, nd)
+    B, hq, d = q.shape
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, hq), dtype=torch.float32, device=q.device)
+    desc = cache_desc(k_pool, page_table, page_size)
+    st = load_library().pkv_decode_attention_static_scratch(
+        ctypes.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(q), hq,
+        _ptr(batch_idx), _ptr(seq_lens), B, float(scale), _ptr(out), _ptr(lse), _ptr(dev_err),
+        _stream(stream))
+    _check("pkv_decode_attention_static_scratch", st)
     return out, lse
 
 
