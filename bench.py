@@ -364,6 +364,47 @@ def run_pkv(args):
         torch.cuda.synchronize()
         return t0.elapsed_time(t1) / steps, h2d, d2h
 
+    def timed_prefill(reps):
+        """Packed prefill of the 64-document workload: the append of its k/v
+        into the pages and the tcgen05 attention, each timed with CUDA events
+        over `reps` back-to-back calls (the inputs, ~430 MB, exceed L2)."""
+        c = W.packed_prefill(0)
+        q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
+        bi, ip = c.batch_idx.to(dev), c.input_pos.to(dev)
+        kp, vp, pt = c.k_pool.to(dev), c.v_pool.to(dev), c.page_table.to(dev)
+        out = torch.empty_like(q)
+        lse = torch.empty((c.n_tokens, c.num_q_heads), dtype=torch.float32, device=dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        for _ in range(3):
+            binding.pkv_append(kp, vp, pt, k, v, bi, ip, c.page_size, dev_err=err)
+            binding.pkv_prefill_attention(q, k, v, bi, ip, c.scale, out=out, lse=lse,
+                                          dev_err=err)
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ev[0].record()
+        for _ in range(reps):
+            binding.pkv_append(kp, vp, pt, k, v, bi, ip, c.page_size, dev_err=err)
+        ev[1].record()
+        for _ in range(reps):
+            binding.pkv_prefill_attention(q, k, v, bi, ip, c.scale, out=out, lse=lse,
+                                          dev_err=err)
+        ev[2].record()
+        torch.cuda.synchronize()
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(err.item()):#x} in prefill")
+        app_us = ev[0].elapsed_time(ev[1]) / reps * 1e3
+        att_us = ev[1].elapsed_time(ev[2]) / reps * 1e3
+        flops = 4.0 * c.head_dim * c.num_q_heads * c.info["pairs"]
+        tf = flops / (att_us * 1e-6) / 1e12
+        return {"workload": f"packed_prefill: 64 documents, lengths U[64,1024], "
+                            f"T={c.n_tokens}, Hq=32, Hkv=8, D=128, seed 0",
+                "attention_call_us": att_us, "algorithmic_flops": flops,
+                "tflops": tf, "bound": "tensor", "peak_tflops": bf16_peak,
+                "frac": tf / bf16_peak, "peak_kind": peak_kind,
+                "append_call_us": app_us,
+                "append_gbs": (c.n_tokens * c.num_kv_heads * c.head_dim * 2 * 4)
+                / (app_us * 1e-6) / 1e9}
+
     case = W.qwen3_b64_decode(0, permute=False)
     bytes_dec = decode_bytes(case)
     kv_only = int(case.seq_lens.long().sum()) * case.num_kv_heads * case.head_dim * 4
@@ -385,6 +426,7 @@ def run_pkv(args):
     perm = W.qwen3_b64_decode(0, permute=True)
     rp = timed_decode(perm, max(args.steps // 4, 10), args.warmup)
     e2e_ms, h2d, d2h = e2e_decode(case, max(args.steps // 10, 10), args.warmup)
+    prefill = timed_prefill(20)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -409,6 +451,7 @@ def run_pkv(args):
         "e2e": {"value": kv_only / (e2e_ms * 1e-3) / 1e9, "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
+        "prefill": prefill,
         "gpu_launches": 3 * args.steps,
         "clocks": r["clocks"],
     }

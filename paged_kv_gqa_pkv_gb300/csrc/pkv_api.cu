@@ -93,7 +93,8 @@ bool group_ok(int num_q_heads, int num_kv_heads) {
   return g == 1 || g == 2 || g == 4 || g == 8;
 }
 
-// 3-D view {D, H_kv, rows} of a token-major pool; a box is 16 rows of one head.
+// 3-D view {D, H_kv, rows} of a token-major pool; a box is 16 rows of one head
+// and half its head dims, 128-byte swizzled (the layout ldmatrix reads).
 pkv_status encode_pool_map(CUtensorMap* map, const void* pool, const pkv_cache_desc* c) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (enc == nullptr) return PKV_ERR_CUDA;
@@ -102,13 +103,13 @@ pkv_status encode_pool_map(CUtensorMap* map, const void* pool, const pkv_cache_d
                               static_cast<cuuint64_t>(c->num_pages) * c->page_size};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(c->head_dim) * 2,
                                  static_cast<cuuint64_t>(c->num_kv_heads) * c->head_dim * 2};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(c->head_dim), 1u,
-                             static_cast<cuuint32_t>(pkv::kDecodeTile)};
+  // 64 head dims x 1 head x 16 tokens: one 128-byte-swizzled half of a tile
+  const cuuint32_t box[3] = {64u, 1u, static_cast<cuuint32_t>(pkv::kDecodeTile)};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
   std::memset(map, 0, sizeof(*map));
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims,
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_ARG;
 }

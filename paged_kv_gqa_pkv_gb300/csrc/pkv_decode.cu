@@ -22,38 +22,52 @@
 // worker + item, unique because both indices grow along the list. The merge
 // kernel combines an item's segments by LSE.
 //
-// Arithmetic per tile (CUDA cores, fp32): all G query heads of a kv head use
-// one load of each K and V row.
-//  * QK: lane (grp = lane/8, j = lane%8) takes token it*4 + grp and dims
-//    {8j..8j+7, 64+8j..64+8j+7} of it, for 4 tokens; the 8 lanes of a group
-//    finish the dot products with a reduce-scatter butterfly (xor 4, 2, 1).
-//  * softmax: scores go through a per-warp shared buffer; the tile max per
-//    head is a warp shuffle reduction; p = exp2(s - m) in place.
-//  * PV: lane owns dims 4*lane..4*lane+3 of all G heads and reads p[t][0..G)
-//    as a broadcast.
+// Arithmetic per tile: all G query heads of a kv head use one load of each K
+// and V row. The two products are small dense contractions
+// (S[G x 16] = Q[G x 128] K^T, O[G x 128] += P[G x 16] V) and run as warp-level
+// bf16 MMAs (m16n8k16, fp32 accumulate) with the G heads as the MMA rows;
+// K and V sit in shared memory in 128-byte-swizzled TMA boxes so ldmatrix
+// reads them without bank conflicts. The online softmax stays in fp32
+// registers: the row max is a quad shuffle reduction, exp2 with the scale
+// folded in, O rescaled only when some row's max moved. P goes from the S
+// accumulators straight into the A operand of the PV product (bf16), so the
+// softmax never touches shared memory. Keys past a row's length are masked to
+// -inf in S and their V rows are zeroed in shared memory before PV (stale
+// slots of a page may hold any bits, NaN included).
 #include "pkv_launch.h"
 
 namespace pkv {
 
 namespace {
 
-constexpr int kKTileBytes = kDecodeTile * kHeadDim * 2;  // one head, 16 tokens
+constexpr int kKTileBytes = kDecodeTile * kHeadDim * 2;  // one head, 16 tokens (4 KB)
 
 template <int G>
 struct DecodeCfg {
   static constexpr int kStages = (G >= 8) ? 2 : kDecodeStages;
   static constexpr int kQBytes = G * kHeadDim * 2;
-  static constexpr int kStageStride = ((2 * kKTileBytes + kQBytes) + 127) / 128 * 128;
+  // stage: K tile (two 2 KB swizzled halves), V tile (same), q rows
+  static constexpr int kOffV = kKTileBytes;
+  static constexpr int kOffQ = 2 * kKTileBytes;
+  static constexpr int kStageStride = ((2 * kKTileBytes + kQBytes) + 1023) / 1024 * 1024;
   static constexpr int kBarOffset = kDecodeWarps * kStages * kStageStride;
-  static constexpr int kScoreOffset = kBarOffset + kDecodeWarps * kStages * 8;
-  static constexpr int kLenOffset = kScoreOffset + kDecodeWarps * kDecodeTile * G * 4;
-  static constexpr int kWarpSumOffset = kLenOffset;  // int[kDecodeWarps]
+  static constexpr int kWarpSumOffset = kBarOffset + kDecodeWarps * kStages * 8;
   static constexpr int kRowsOffset = kWarpSumOffset + kDecodeWarps * 4;
   static constexpr size_t smem_bytes(int batch) {
-    // seq_len per row, then the tile prefix over rows ([batch + 1])
-    return kRowsOffset + static_cast<size_t>(batch) * 4 + static_cast<size_t>(batch + 1) * 4;
+    // + 1 KB to round the dynamic base up to the swizzle-atom alignment
+    return 1024 + kRowsOffset + static_cast<size_t>(batch) * 4 +
+           static_cast<size_t>(batch + 1) * 4;
   }
 };
+
+constexpr int kHalfBytes = kDecodeTile * 128;  // 16 rows x 64 dims (bf16) TMA box
+
+// Byte offset of 16-byte chunk `chunk` (0..15, eight dims each) of row `row`
+// inside a [16 rows x 128 dims] tile stored as two 128-byte-swizzled halves.
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return static_cast<uint32_t>((chunk >> 3) * kHalfBytes + row * 128 +
+                               (((chunk & 7) ^ (row & 7)) << 4));
+}
 
 // Position of a worker inside the tile list.
 struct Cursor {
@@ -139,7 +153,10 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
   using C = DecodeCfg<G>;
   constexpr int S = C::kStages;
-  extern __shared__ __align__(128) uint8_t smem[];
+  static_assert(G <= 8, "GQA group must fit the MMA's 16 rows with the q rows of one head group");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -149,7 +166,6 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
 
   uint8_t* stages = smem + warp * S * C::kStageStride;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset) + warp * S;
-  float* s_score = reinterpret_cast<float*>(smem + C::kScoreOffset) + warp * kDecodeTile * G;
   int* s_warp_sum = reinterpret_cast<int*>(smem + C::kWarpSumOffset);
   int32_t* s_len = reinterpret_cast<int32_t*>(smem + C::kRowsOffset);
   int32_t* s_prefix = s_len + B;
@@ -243,12 +259,14 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
       const bool seg_start = (k == 0) || (c.tile == 0);
       mbar_arrive_expect_tx(&bars[s], 2 * kKTileBytes + (seg_start ? C::kQBytes : 0));
       tma_load_3d(st, &kmap, &bars[s], 0, c.kvh, row);
-      tma_load_3d(st + kKTileBytes, &vmap, &bars[s], 0, c.kvh, row);
+      tma_load_3d(st + kHalfBytes, &kmap, &bars[s], 64, c.kvh, row);
+      tma_load_3d(st + C::kOffV, &vmap, &bars[s], 0, c.kvh, row);
+      tma_load_3d(st + C::kOffV + kHalfBytes, &vmap, &bars[s], 64, c.kvh, row);
       if (seg_start) {
         const size_t qoff =
             (static_cast<size_t>(c.b) * p.num_q_heads + static_cast<size_t>(c.kvh) * G) *
             kHeadDim * 2;
-        bulk_load(st + 2 * kKTileBytes, qbase + qoff, C::kQBytes, &bars[s]);
+        bulk_load(st + C::kOffQ, qbase + qoff, C::kQBytes, &bars[s]);
       }
     }
   };
@@ -259,14 +277,19 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
     if (k + 1 < count) advance(pc, s_prefix, hkv);
   }
 
-  const int grp = lane >> 3;
-  const int jl = lane & 7;
-  const int hg = lane % G;  // head whose softmax statistics this lane keeps
-  float q[G][16];
-  float acc[G][4];
+  // MMA fragment coordinates: g = row (query head) of this lane's accumulators,
+  // t = its column pair.
+  const int g = lane >> 2;
+  const int t = lane & 3;
+  const bool live_row = g < G;
+  uint32_t qa[8][2];     // A fragments of q (rows 0..G-1; rows >= G are zero)
+  float acc[16][4];      // O accumulators, n-tile = 8 head dims
   float m_run = -INFINITY, l_run = 0.f;
   int n_row = 0;
   int issued = prologue;
+  // ldmatrix row addresses (per lane) within a K or V tile
+  const int mtx = lane >> 3;       // which of the four 8x8 matrices this lane addresses
+  const int mrow = lane & 7;
 
   for (int k = 0; k < count; ++k) {
     const int s = k % S;
@@ -275,157 +298,110 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
       bail = true;
       break;
     }
-    const uint8_t* st = stages + s * C::kStageStride;
+    uint8_t* st = stages + s * C::kStageStride;
+    const uint32_t sK = smem_u32(st);
+    const uint32_t sV = smem_u32(st + C::kOffV);
     const bool seg_start = (k == 0) || (cc.tile == 0);
     if (seg_start) {
-      const uint8_t* qs = st + 2 * kKTileBytes;
+      const uint32_t* qs = reinterpret_cast<const uint32_t*>(st + C::kOffQ);
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const uint4 a = *reinterpret_cast<const uint4*>(qs + g * 256 + jl * 16);
-        const uint4 c = *reinterpret_cast<const uint4*>(qs + g * 256 + 128 + jl * 16);
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          q[g][2 * e] = bf16lo(w[e]) * p.qscale;
-          q[g][2 * e + 1] = bf16hi(w[e]) * p.qscale;
-        }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[g][e] = 0.f;
+      for (int kk = 0; kk < 8; ++kk) {
+        qa[kk][0] = live_row ? qs[g * 64 + kk * 8 + t] : 0u;
+        qa[kk][1] = live_row ? qs[g * 64 + kk * 8 + 4 + t] : 0u;
       }
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
       m_run = -INFINITY;
       l_run = 0.f;
       n_row = s_len[cc.b];
     }
     const int n_valid = min(kDecodeTile, n_row - cc.tile * kDecodeTile);
 
-    // ---- QK: partial dot products over this lane's 16 dims ----
-    constexpr int N = 4 * G;
-    float v[N];
-    const uint8_t* ks = st;
+    // ---- S = Q K^T: two n-tiles of 8 tokens, 8 k-steps of 16 dims ----
+    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int t = it * 4 + grp;
-      const uint4 a = *reinterpret_cast<const uint4*>(ks + t * 256 + jl * 16);
-      const uint4 c = *reinterpret_cast<const uint4*>(ks + t * 256 + 128 + jl * 16);
-      const uint32_t w[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-      float kf[16];
+    for (int kk = 0; kk < 8; ++kk) {
+      uint32_t b0, b1, b2, b3;
+      // matrices: (tokens 0-7 | 8-15) x (dims 16kk..+7 | 16kk+8..+15)
+      ldsm_x4(sK + swz((mtx >> 1) * 8 + mrow, 2 * kk + (mtx & 1)), b0, b1, b2, b3);
+      mma_16816(sc[0], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+      mma_16816(sc[1], qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
+    }
+    // ---- online softmax (log2 units) on rows g; columns t*2, t*2+1 (+8) ----
+    float x[4] = {sc[0][0] * p.qscale, sc[0][1] * p.qscale, sc[1][0] * p.qscale,
+                  sc[1][1] * p.qscale};
+    if (n_valid < kDecodeTile) {
+      const int tok[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        kf[2 * e] = bf16lo(w[e]);
-        kf[2 * e + 1] = bf16hi(w[e]);
+      for (int e = 0; e < 4; ++e)
+        if (tok[e] >= n_valid) x[e] = -INFINITY;
+      // stale slots past the row's end: zero their V rows before PV
+      for (int r = n_valid; r < kDecodeTile; ++r) {
+        uint4* vrow = reinterpret_cast<uint4*>(st + C::kOffV);
+        if (lane < 16) vrow[(swz(r, lane)) >> 4] = make_uint4(0u, 0u, 0u, 0u);
       }
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float d0 = 0.f, d1 = 0.f;
-#pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          d0 = fmaf(q[g][e], kf[e], d0);
-          d1 = fmaf(q[g][e + 1], kf[e + 1], d1);
-        }
-        v[it * G + g] = d0 + d1;
-      }
+      __syncwarp();
     }
-    // ---- reduce-scatter across the 8 lanes of the group ----
-    int idx0 = 0;
-    rs_step<N / 2, 4>(v, lane, idx0);
-    rs_step<N / 4, 2>(v, lane, idx0);
-    if constexpr (N / 4 >= 2) {
-      rs_step<N / 8, 1>(v, lane, idx0);
-    } else {
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
-    }
-    constexpr int kHeld = (N >= 8) ? N / 8 : 1;
-#pragma unroll
-    for (int i = 0; i < kHeld; ++i) {
-      const int idx = idx0 + i;
-      const int t = (idx / G) * 4 + grp;
-      const int g = idx % G;
-      s_score[t * G + g] = (t < n_valid) ? v[i] : -INFINITY;
-    }
-    __syncwarp();
-
-    // ---- online softmax (log2 units) ----
-    constexpr int kPer = (kDecodeTile * G + 31) / 32;
-    constexpr int kStride = 32 / G;
-    float sv[kPer];
-    float mx = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int t = lane / G + i * kStride;
-      sv[i] = (t < kDecodeTile) ? s_score[t * G + hg] : -INFINITY;
-      mx = fmaxf(mx, sv[i]);
-    }
-#pragma unroll
-    for (int m = G; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
     const float m_new = fmaxf(m_run, mx);
-    const float alpha = exp2f(m_run - m_new);
-    float psum = 0.f;
+    const float alpha = exp2f(m_run - m_new);  // 0 on the first tile
+    float pe[4];
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int t = lane / G + i * kStride;
-      if (t < kDecodeTile) {
-        const float pv = exp2f(sv[i] - m_new);
-        s_score[t * G + hg] = pv;
-        psum += pv;
-      }
-    }
-    l_run = l_run * alpha + psum;
+    for (int e = 0; e < 4; ++e) pe[e] = exp2f(x[e] - m_new);
+    l_run = l_run * alpha + ((pe[0] + pe[1]) + (pe[2] + pe[3]));
     m_run = m_new;
-    __syncwarp();
+    if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float a = __shfl_sync(0xffffffffu, alpha, g);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[g][e] *= a;
+      for (int nt = 0; nt < 16; ++nt) {
+        acc[nt][0] *= alpha;
+        acc[nt][1] *= alpha;
+      }
     }
+    const uint32_t pa0 = pack_bf16x2(pe[0], pe[1]);  // P[g][2t..2t+1]
+    const uint32_t pa2 = pack_bf16x2(pe[2], pe[3]);  // P[g][8+2t..9+2t]
 
-    // ---- PV over the valid tokens ----
-    const uint8_t* vs = st + kKTileBytes;
-#pragma unroll 4
-    for (int t = 0; t < n_valid; ++t) {
-      const uint2 w = *reinterpret_cast<const uint2*>(vs + t * 256 + lane * 8);
-      const float v0 = bf16lo(w.x), v1 = bf16hi(w.x), v2 = bf16lo(w.y), v3 = bf16hi(w.y);
-      float pg[G];
-      if constexpr (G % 4 == 0) {
+    // ---- O += P V: 16 n-tiles of 8 dims, one k-step of 16 tokens ----
 #pragma unroll
-        for (int g = 0; g < G; g += 4) {
-          const float4 p4 = *reinterpret_cast<const float4*>(s_score + t * G + g);
-          pg[g] = p4.x; pg[g + 1] = p4.y; pg[g + 2] = p4.z; pg[g + 3] = p4.w;
-        }
-      } else {
-#pragma unroll
-        for (int g = 0; g < G; ++g) pg[g] = s_score[t * G + g];
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        acc[g][0] = fmaf(pg[g], v0, acc[g][0]);
-        acc[g][1] = fmaf(pg[g], v1, acc[g][1]);
-        acc[g][2] = fmaf(pg[g], v2, acc[g][2]);
-        acc[g][3] = fmaf(pg[g], v3, acc[g][3]);
-      }
+    for (int np = 0; np < 8; ++np) {
+      uint32_t b0, b1, b2, b3;
+      // matrices: (tokens 0-7 | 8-15) x (dims 16np..+7 | 16np+8..+15), transposed
+      ldsm_x4_trans(sV + swz((mtx & 1) * 8 + mrow, 2 * np + (mtx >> 1)), b0, b1, b2, b3);
+      mma_16816(acc[2 * np], pa0, 0u, pa2, 0u, b0, b1);
+      mma_16816(acc[2 * np + 1], pa0, 0u, pa2, 0u, b2, b3);
     }
 
     // ---- segment end: leave the partial in slot worker + item ----
     const bool seg_end = (k == count - 1) || (cc.tile == cc.tiles - 1);
     if (seg_end) {
       float lt = l_run;
-#pragma unroll
-      for (int m = G; m < 32; m <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, m);
+      lt += __shfl_xor_sync(0xffffffffu, lt, 1);
+      lt += __shfl_xor_sync(0xffffffffu, lt, 2);
       const int64_t slot_id = static_cast<int64_t>(worker) + static_cast<int64_t>(cc.b) * hkv + cc.kvh;
       float* slot = p.partials + slot_id * decode_slot_floats(G);
+      if (live_row) {
 #pragma unroll
-      for (int g = 0; g < G; ++g)
-        *reinterpret_cast<float4*>(slot + g * kHeadDim + lane * 4) =
-            make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
-      if (lane < G) {
-        slot[G * kHeadDim + lane] = m_run;
-        slot[G * kHeadDim + G + lane] = lt;
+        for (int nt = 0; nt < 16; ++nt)
+          *reinterpret_cast<float2*>(slot + g * kHeadDim + nt * 8 + 2 * t) =
+              make_float2(acc[nt][0], acc[nt][1]);
+        if (t == 0) {
+          slot[G * kHeadDim + g] = m_run;
+          slot[G * kHeadDim + G + g] = lt;
+        }
       }
     }
     __syncwarp();
 
     // ---- refill this stage with the tile S ahead ----
     if (k + S < count) {
+      if (n_valid < kDecodeTile) {
+        // V rows zeroed above (generic proxy) must land before TMA refills them
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
       issue(pc, k + S);
       ++issued;
       if (k + S + 1 < count) advance(pc, s_prefix, hkv);
