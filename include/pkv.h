@@ -115,6 +115,7 @@ size_t pkv_decode_workspace_size(const pkv_cache_desc* cache, int batch,
  * (enable_gqa); zero-safe padded rows: "flex_vs_vllm.md", "What broke
  * correctness and had to be dropped" (ROWS_GUARANTEED_SAFE).
  *
+ * batch may be 0..512 per call (larger batches: split them over calls).
  * Row b in [0, batch) has one query token q[b] (bf16 [num_q_heads, D] within
  * a contiguous [batch, num_q_heads, D] tensor) and attends the first
  * n = seq_lens[b] logical keys of slot c = batch_idx[b] (for a decode step

@@ -18,10 +18,10 @@ constexpr int kAppendWarps = 8;
 
 __global__ void __launch_bounds__(kAppendWarps * 32)
 append_kernel(AppendParams p) {
-  // Let a dependent decode launch start its CTAs; it still waits for this
-  // grid's completion before it reads anything.
-  pdl_launch_dependents();
+  // Launched as a programmatic dependent: wait for the previous kernel (it may
+  // still read the pools), then let the next launch start its prologue.
   pdl_wait_primary();
+  pdl_launch_dependents();
 
   const int lane = threadIdx.x & 31;
   const int i = blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
@@ -60,7 +60,7 @@ append_kernel(AppendParams p) {
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
   const int grid = (p.n_tokens + kAppendWarps - 1) / kAppendWarps;
   return launch_kernel(append_kernel, dim3(grid), dim3(kAppendWarps * 32), 0, stream,
-                       /*programmatic=*/false, p);
+                       /*programmatic=*/true, p);
 }
 
 }  // namespace pkv

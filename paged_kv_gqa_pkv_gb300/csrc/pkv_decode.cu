@@ -54,8 +54,9 @@ struct DecodeCfg {
   static constexpr int kWarpSumOffset = kBarOffset + kDecodeWarps * kStages * 8;
   static constexpr int kRowsOffset = kWarpSumOffset + kDecodeWarps * 4;
   static constexpr size_t smem_bytes(int batch) {
-    // + 1 KB to round the dynamic base up to the swizzle-atom alignment
-    return 1024 + kRowsOffset + static_cast<size_t>(batch) * 4 +
+    // seq_len and slot per row, the tile prefix over rows ([batch + 1]), and
+    // 1 KB to round the dynamic base up to the swizzle-atom alignment
+    return 1024 + kRowsOffset + static_cast<size_t>(batch) * 8 +
            static_cast<size_t>(batch + 1) * 4;
   }
 };
@@ -128,10 +129,11 @@ struct RowPages {
   bool contiguous;  // page_table[slot, j] == base + j for every needed block
 };
 
-__device__ __forceinline__ void load_row_pages(RowPages& rp, const DecodeParams& p, int b,
-                                               int tiles, int lane) {
+__device__ __forceinline__ void load_row_pages(RowPages& rp, const DecodeParams& p,
+                                               const int32_t* s_slot, int b, int tiles,
+                                               int lane) {
   rp.b = b;
-  rp.slot = p.batch_idx[b];
+  rp.slot = s_slot[b];
   const int32_t* row = p.page_table + static_cast<int64_t>(rp.slot) * p.max_blocks;
   const int nblk = (tiles * kDecodeTile + p.page_size - 1) / p.page_size;
   const int base = row[0];
@@ -168,7 +170,8 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOffset) + warp * S;
   int* s_warp_sum = reinterpret_cast<int*>(smem + C::kWarpSumOffset);
   int32_t* s_len = reinterpret_cast<int32_t*>(smem + C::kRowsOffset);
-  int32_t* s_prefix = s_len + B;
+  int32_t* s_slot = s_len + B;
+  int32_t* s_prefix = s_slot + B;
 
   if (lane == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
@@ -178,8 +181,10 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
     tma_prefetch_desc(&kmap);
     tma_prefetch_desc(&vmap);
   }
-  // Everything read below may be written by the previous kernel on the stream.
-  pdl_wait_primary();
+  // Programmatic dependent launch: this prologue (row lengths, slots, the tile
+  // prefix, the first page-table row) reads only arrays that no kernel of this
+  // library writes, so it overlaps the previous kernel on the stream; the
+  // pools, q and the workspace are touched only after pdl_wait_primary().
   pdl_launch_dependents();
 
   // ---- tiles per row and their exclusive prefix sum (every CTA, in smem) ----
@@ -197,6 +202,7 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
     else if (c != 0) tiles = (n + kDecodeTile - 1) / kDecodeTile;
     if (err && blockIdx.x == 0) set_dev_err(p.dev_err, err);
     s_len[r] = n;
+    s_slot[r] = c;
     s_prefix[r] = tiles;
     local += tiles;
   }
@@ -217,9 +223,6 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
   }
   if (tid == blockDim.x - 1) s_prefix[B] = run;
   __syncthreads();
-  if (blockIdx.x == 0) {
-    for (int r = tid; r <= B; r += blockDim.x) p.prefix[r] = s_prefix[r];
-  }
 
   // ---- this warp's range of the tile list ----
   const int64_t total = static_cast<int64_t>(s_prefix[B]) * hkv;
@@ -227,7 +230,13 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
   const int64_t per = (total + p.num_workers - 1) / p.num_workers;
   const int64_t u_begin = static_cast<int64_t>(worker) * per;
   const int64_t u_end = min(u_begin + per, total);
-  if (u_begin >= u_end) return;
+  if (u_begin >= u_end) {
+    if (blockIdx.x == 0 && warp == 0) {
+      pdl_wait_primary();
+      for (int r = lane; r <= B; r += 32) p.prefix[r] = s_prefix[r];
+    }
+    return;
+  }
   const int count = static_cast<int>(u_end - u_begin);
 
   const Cursor start = locate(s_prefix, B, hkv, u_begin);
@@ -239,7 +248,7 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
 
   const uint8_t* qbase = static_cast<const uint8_t*>(p.q);
   auto issue = [&](const Cursor& c, int k) {
-    if (c.b != rp.b) load_row_pages(rp, p, c.b, c.tiles, lane);
+    if (c.b != rp.b) load_row_pages(rp, p, s_slot, c.b, c.tiles, lane);
     if (lane == 0) {
       const int s = k % S;
       uint8_t* st = stages + s * C::kStageStride;
@@ -271,6 +280,11 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
     }
   };
 
+  load_row_pages(rp, p, s_slot, start.b, start.tiles, lane);
+  pdl_wait_primary();
+  if (blockIdx.x == 0 && warp == 0) {
+    for (int r = lane; r <= B; r += 32) p.prefix[r] = s_prefix[r];
+  }
   const int prologue = min(S, count);
   for (int k = 0; k < prologue; ++k) {
     issue(pc, k);
@@ -423,6 +437,9 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
 // combination is a warp reduction.
 template <int G>
 __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p) {
+  // The next launch may start its prologue now; it touches the workspace
+  // only after this grid completes.
+  pdl_launch_dependents();
   pdl_wait_primary();
   const int lane = threadIdx.x & 31;
   const int wid = blockIdx.x * 8 + (threadIdx.x >> 5);

@@ -56,7 +56,7 @@ struct DecodeParams {
 constexpr int kDecodeTile = 16;       // tokens per pipeline stage
 constexpr int kDecodeWarps = 8;       // workers (warps) per CTA
 constexpr int kDecodeStages = 3;      // stages in flight per worker
-constexpr int kDecodeMaxBatch = 1024; // rows per call (prefix lives in smem)
+constexpr int kDecodeMaxBatch = 512;  // rows per call (row tables live in smem)
 
 // Floats per partial slot: unnormalised o[G][D], then m[G], l[G] (padded).
 __host__ __device__ constexpr int decode_slot_floats(int g) {

@@ -11,18 +11,21 @@
 // numbered 0, 1, 2, ...; then the keys of query i are exactly the packed rows
 // [i - input_pos[i], i]. A row that breaks it sets PKV_DEV_ERR_LAYOUT.
 //
-// One CTA computes a 128-row query tile for one query head:
-//  * warp 0 issues TMA loads: the Q tile once, then K/V tiles of 128 keys
-//    into a two-stage ring, starting at the first key any row of the tile
-//    can see (KV tiles outside the tile's documents are never loaded);
-//  * warp 1 (one thread) issues the tcgen05 MMAs: S = Q K^T into one of two
-//    TMEM buffers (the next S is computed while the current one is in
-//    softmax), then O += P V into a TMEM accumulator;
-//  * warps 2..5 own one query row per thread (its TMEM lane): masked online
-//    softmax in fp32 (exp2 with the scale folded in), P written to shared
-//    memory as bf16 in the MMA's K-major 128-byte-swizzled layout, O rescaled
-//    in TMEM only when the running max grows by more than 2^8, and the
-//    epilogue O / l -> bf16 plus the LSE.
+// Schedule: a persistent grid (one CTA per SM) walks the work items
+// round-robin; an item is one 128-row query tile for TWO query heads of the
+// same GQA group, so every K/V tile is loaded once for both heads (a group of
+// one head, G == 1, gives one-head items). Warp roles:
+//  * warp 0 issues TMA: each item's Q tiles, then K and V tiles of 128 keys
+//    into a 3-slot ring of 32 KB half-stages (K_j, V_j, K_j+1, ... in order,
+//    across items), starting at the first key any row of the tile can see;
+//  * warp 1 (one thread) issues tcgen05 MMAs: S_h = Q_h K^T into TMEM and
+//    O_h += P_h V, interleaved so one head's softmax overlaps the other's MMAs;
+//  * warps 2..5 and 6..9 are the softmax warpgroups of the two heads, one
+//    query row per thread (its TMEM lane): masked online softmax in fp32 with
+//    exp2 and the scale folded in, P written to shared memory as bf16 in the
+//    MMA's K-major 128-byte-swizzled layout, O rescaled in TMEM only when the
+//    running max grows by more than 2^8, and the epilogue O / l -> bf16 + LSE.
+// Barrier phases are running counters kept identically by every role.
 // Shared-memory operands (all 128-byte swizzled, 1024-byte aligned atoms):
 // Q, K and P are K-major (64 elements per 128-byte row, two 16 KB halves of
 // D or of the key block); V is used MN-major straight from its TMA tile
@@ -38,24 +41,23 @@ namespace {
 constexpr int kBM = 128;                 // query rows per tile
 constexpr int kBN = 128;                 // keys per KV tile
 constexpr int kHalf = 128 * 128;         // one [128 rows x 64 elems] bf16 block, bytes
-constexpr int kTileBytes = 2 * kHalf;    // 128 x 128 bf16
-constexpr int kStages = 2;
-constexpr int kThreads = 6 * 32;
-constexpr int kSoftmaxThreads = 128;
-constexpr uint32_t kTmemCols = 512;      // S0 [0,128) S1 [128,256) O [256,384)
-constexpr uint32_t kColO = 256;
+constexpr int kTileBytes = 2 * kHalf;    // 128 x 128 bf16 (32 KB)
+constexpr int kRing = 3;                 // K/V half-stage slots
+constexpr int kThreads = 10 * 32;
+constexpr int kGroupThreads = 128;       // one softmax warpgroup
+constexpr uint32_t kTmemCols = 512;      // S0 S1 O0 O1, 128 columns each
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 // shared memory layout (offsets from a 1024-aligned base)
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTileBytes;
-constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffP = kOffV + kStages * kTileBytes;
-constexpr int kOffBar = kOffP + kTileBytes;
-// barriers: q_full, kv_full[2], kv_empty[2], s_full[2], p_full, pv_done
-constexpr int kNumBars = 9;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;   // tmem slot, kv_lo, kv_hi, abort
-constexpr int kSmemBytes = kOffMisc + 64 + 1024;   // + slack for 1024 alignment
+constexpr int kOffQ = 0;                              // Q0, Q1
+constexpr int kOffP = kOffQ + 2 * kTileBytes;         // P0, P1
+constexpr int kOffRing = kOffP + 2 * kTileBytes;      // 3 slots
+constexpr int kOffBar = kOffRing + kRing * kTileBytes;
+// q_full, q_empty, ring_full[3], ring_empty[3], s_full[2], p_full[2],
+// pv_done[2], o_free[2]
+constexpr int kNumBars = 16;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;      // tmem slot, abort flag
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;      // + slack for 1024 alignment
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, /*b_mn_major=*/false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kHeadDim, /*b_mn_major=*/true);
@@ -69,10 +71,57 @@ struct PrefillParams {
   int n_tokens;
   int num_q_heads;
   int group;
-  float qscale;  // scale * log2(e)
+  int heads_per_item;   // 2 when group >= 2, else 1
+  int n_tiles;          // query tiles
+  int n_items;          // n_tiles * num_q_heads / heads_per_item
+  float qscale;         // scale * log2(e)
 };
 
-__device__ __forceinline__ bool aborted(volatile int* flag) { return *flag != 0; }
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Keys [kv_lo, kv_hi) that rows r0..r0+127 can see: one warp, four rows per
+// lane. Under the packing precondition a valid row i sees [i - pos_i, i].
+__device__ __forceinline__ void tile_key_range(const PrefillParams& p, int r0, int lane,
+                                               int& kv_lo, int& kv_hi) {
+  int lo = 0x7fffffff, hi = -1;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int i = r0 + lane + 32 * m;
+    if (i < p.n_tokens && p.batch_idx[i] != 0) {
+      const int pos = p.input_pos[i];
+      lo = min(lo, (pos >= 0 && pos <= i) ? i - pos : i);
+      hi = max(hi, i + 1);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  kv_lo = lo;
+  kv_hi = hi;
+}
+
+// Bounded wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
+                                              volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
 
 }  // namespace
 
@@ -85,40 +134,38 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;    // [2]
-  uint64_t* p_full = bars + 7;
-  uint64_t* pv_done = bars + 8;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* ring_full = bars + 2;   // [3]
+  uint64_t* ring_empty = bars + 5;  // [3]
+  uint64_t* s_full = bars + 8;      // [2]
+  uint64_t* p_full = bars + 10;     // [2]
+  uint64_t* pv_done = bars + 12;    // [2]
+  uint64_t* o_free = bars + 14;     // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  int* s_kv_lo = reinterpret_cast<int*>(smem + kOffMisc + 4);
-  int* s_kv_hi = reinterpret_cast<int*>(smem + kOffMisc + 8);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 12);
-  int* s_skip = reinterpret_cast<int*>(smem + kOffMisc + 16);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int head = blockIdx.x % p.num_q_heads;
-  const int tile = blockIdx.x / p.num_q_heads;
-  const int kvh = head / p.group;
-  const int r0 = tile * kBM;
+  const int hpi = p.heads_per_item;
+  const int items_per_tile = p.num_q_heads / hpi;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
-      mbar_init(&s_full[s], 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&ring_full[s], 1);
+      mbar_init(&ring_empty[s], 1);
     }
-    mbar_init(p_full, kSoftmaxThreads);
-    mbar_init(pv_done, 1);
-    *s_kv_lo = 0x7fffffff;
-    *s_kv_hi = -1;
-    *s_abort = 0;
-    // After a timeout anywhere in the grid, later CTAs do no work (their
-    // results are unspecified then) instead of each waiting out its limit.
-    *s_skip = (p.dev_err != nullptr &&
-               (*reinterpret_cast<volatile int32_t*>(p.dev_err) & PKV_DEV_ERR_TIMEOUT)) ? 1 : 0;
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&s_full[h], 1);
+      mbar_init(&p_full[h], kGroupThreads);
+      mbar_init(&pv_done[h], 1);
+      mbar_init(&o_free[h], kGroupThreads);
+    }
+    // After a timeout anywhere in the grid, this CTA does no work (results
+    // are unspecified then) instead of waiting out its own limits.
+    *s_abort = (p.dev_err != nullptr &&
+                (*reinterpret_cast<volatile int32_t*>(p.dev_err) & PKV_DEV_ERR_TIMEOUT)) ? 1 : 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -127,247 +174,312 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
     tma_prefetch_desc(&vmap);
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
-
-  // ---- per-row document bounds (softmax threads), CTA-wide key range ----
-  const bool is_softmax = warp >= 2;
-  const int lane_base = 32 * (warp & 3);  // TMEM lanes this warp may access
-  const int row = lane_base + lane;       // query row within the tile
-  const int i = r0 + row;                 // packed token index
-  bool valid = false;
-  int start = 0;
-  if (is_softmax && i < p.n_tokens) {
-    const int b = p.batch_idx[i];
-    const int pos = p.input_pos[i];
-    if (b != 0) {
-      valid = true;
-      bool ok = pos >= 0 && pos <= i;
-      if (ok && pos > 0) ok = (p.batch_idx[i - 1] == b) && (p.input_pos[i - 1] == pos - 1);
-      if (!ok) set_dev_err(p.dev_err, PKV_DEV_ERR_LAYOUT);
-      start = (pos >= 0 && pos <= i) ? i - pos : i;
-      atomicMin(s_kv_lo, start);
-      atomicMax(s_kv_hi, i + 1);
-    }
-  }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int kv_lo = *s_kv_lo;
-  const int kv_hi = *s_kv_hi;
-  const int n_kv = (kv_hi > kv_lo && *s_skip == 0) ? (kv_hi - kv_lo + kBN - 1) / kBN : 0;
 
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer ----
-    if (lane == 0 && n_kv > 0) {
-      mbar_arrive_expect_tx(q_full, kTileBytes);
-      tma_load_3d(smem + kOffQ, &qmap, q_full, 0, head, r0);
-      tma_load_3d(smem + kOffQ + kHalf, &qmap, q_full, 64, head, r0);
-      for (int j = 0; j < n_kv; ++j) {
-        const int s = j % kStages;
-        if (j >= kStages && !mbar_wait_bounded(&kv_empty[s], ((j / kStages) - 1) & 1)) {
-          set_dev_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-          *s_abort = 1;
-          break;
+    // ---------------------------------------------------- TMA producer ----
+    uint32_t L = 0;   // ring loads issued
+    uint32_t qi = 0;  // non-empty items
+    for (int item = blockIdx.x; item < p.n_items && !*s_abort; item += gridDim.x) {
+      const int tile = item / items_per_tile;
+      const int h0 = (item % items_per_tile) * hpi;
+      const int kvh = h0 / p.group;
+      const int r0 = tile * kBM;
+      int kv_lo, kv_hi;
+      tile_key_range(p, r0, lane, kv_lo, kv_hi);
+      if (kv_hi <= kv_lo) continue;
+      const int n_kv = (kv_hi - kv_lo + kBN - 1) / kBN;
+      if (lane == 0) {
+        bool ok = qi == 0 || wait_or_abort(q_empty, (qi - 1) & 1, s_abort);
+        if (ok) {
+          mbar_arrive_expect_tx(q_full, hpi * kTileBytes);
+          for (int h = 0; h < hpi; ++h) {
+            uint8_t* qd = smem + kOffQ + h * kTileBytes;
+            tma_load_3d(qd, &qmap, q_full, 0, h0 + h, r0);
+            tma_load_3d(qd + kHalf, &qmap, q_full, 64, h0 + h, r0);
+          }
         }
-        const int krow = kv_lo + j * kBN;
-        uint8_t* kd = smem + kOffK + s * kTileBytes;
-        uint8_t* vd = smem + kOffV + s * kTileBytes;
-        mbar_arrive_expect_tx(&kv_full[s], 2 * kTileBytes);
-        tma_load_3d(kd, &kmap, &kv_full[s], 0, kvh, krow);
-        tma_load_3d(kd + kHalf, &kmap, &kv_full[s], 64, kvh, krow);
-        tma_load_3d(vd, &vmap, &kv_full[s], 0, kvh, krow);
-        tma_load_3d(vd + kHalf, &vmap, &kv_full[s], 64, kvh, krow);
+        for (int j = 0; ok && j < n_kv; ++j) {
+          for (int part = 0; part < 2 && ok; ++part) {
+            const uint32_t slot = L % kRing;
+            if (L >= kRing && !wait_or_abort(&ring_empty[slot], ((L / kRing) - 1) & 1, s_abort)) {
+              ok = false;
+              break;
+            }
+            uint8_t* dst = smem + kOffRing + slot * kTileBytes;
+            const CUtensorMap* map = part == 0 ? &kmap : &vmap;
+            mbar_arrive_expect_tx(&ring_full[slot], kTileBytes);
+            tma_load_3d(dst, map, &ring_full[slot], 0, kvh, kv_lo + j * kBN);
+            tma_load_3d(dst + kHalf, map, &ring_full[slot], 64, kvh, kv_lo + j * kBN);
+            ++L;
+          }
+        }
+        if (!ok) *s_abort = 1;
       }
+      __syncwarp();
+      ++qi;
     }
   } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer ----
-    if (lane == 0 && n_kv > 0) {
-      const uint32_t sQ = smem_u32(smem + kOffQ);
-      const uint32_t sP = smem_u32(smem + kOffP);
-      auto issue_qk = [&](int j) {
-        const int s = j % kStages;
-        const uint32_t sK = smem_u32(smem + kOffK + s * kTileBytes);
-        const uint32_t d = tmem + static_cast<uint32_t>((j & 1) * kBN);
+    // ------------------------------------------------------ MMA issuer ----
+    uint32_t C = 0;       // ring slots consumed
+    uint32_t qi = 0;      // non-empty items
+    uint32_t tc = 0;      // KV tiles processed (all items)
+    const uint32_t sQ = smem_u32(smem + kOffQ);
+    const uint32_t sP = smem_u32(smem + kOffP);
+    const uint32_t sR = smem_u32(smem + kOffRing);
+    auto qk = [&](int h, uint32_t kslot) {
+      const uint32_t q = sQ + h * kTileBytes;
+      const uint32_t k = sR + kslot * kTileBytes;
+      const uint32_t d = tmem + static_cast<uint32_t>(h * kBN);  // S_h
 #pragma unroll
-        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          umma_bf16(d, sw128_desc(sQ + off, 0, 1024), sw128_desc(sK + off, 0, 1024), kIdescQK,
-                    kk > 0 ? 1u : 0u);
-        }
-        umma_commit(&s_full[j & 1]);
-      };
-      bool ok = mbar_wait_bounded(q_full, 0) && mbar_wait_bounded(&kv_full[0], 0);
-      if (ok) {
-        tc_fence_after();
-        issue_qk(0);
+      for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+        umma_bf16(d, sw128_desc(q + off, 0, 1024), sw128_desc(k + off, 0, 1024), kIdescQK,
+                  kk > 0 ? 1u : 0u);
       }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        if (j + 1 < n_kv) {
-          const int s1 = (j + 1) % kStages;
-          if (!mbar_wait_bounded(&kv_full[s1], ((j + 1) / kStages) & 1)) { ok = false; break; }
-          tc_fence_after();
-          issue_qk(j + 1);
-        }
-        if (!mbar_wait_bounded(p_full, j & 1)) { ok = false; break; }
-        tc_fence_after();
-        const int s = j % kStages;
-        const uint32_t sV = smem_u32(smem + kOffV + s * kTileBytes);
+      umma_commit(&s_full[h]);
+    };
+    auto pv = [&](int h, uint32_t vslot, bool accumulate) {
+      const uint32_t pp = sP + h * kTileBytes;
+      const uint32_t v = sR + vslot * kTileBytes;
+      const uint32_t d = tmem + static_cast<uint32_t>(256 + h * kHeadDim);  // O_h
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint32_t a_off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          umma_bf16(tmem + kColO, sw128_desc(sP + a_off, 0, 1024),
-                    sw128_desc(sV + kk * 2048, kHalf, 1024), kIdescPV,
-                    (j > 0 || kk > 0) ? 1u : 0u);
+      for (int kk = 0; kk < kBN / 16; ++kk) {
+        const uint32_t a_off = (kk >> 2) * kHalf + (kk & 3) * 32;
+        umma_bf16(d, sw128_desc(pp + a_off, 0, 1024), sw128_desc(v + kk * 2048, kHalf, 1024),
+                  kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+      }
+      umma_commit(&pv_done[h]);
+    };
+    for (int item = blockIdx.x; item < p.n_items && !*s_abort; item += gridDim.x) {
+      const int r0 = (item / items_per_tile) * kBM;
+      int kv_lo, kv_hi;
+      tile_key_range(p, r0, lane, kv_lo, kv_hi);
+      if (kv_hi <= kv_lo) continue;
+      const int n_kv = (kv_hi - kv_lo + kBN - 1) / kBN;
+      if (lane == 0) {
+        bool ok = wait_or_abort(q_full, qi & 1, s_abort);
+        uint32_t kslot = C % kRing;
+        ok = ok && wait_or_abort(&ring_full[kslot], (C / kRing) & 1, s_abort);
+        ++C;
+        if (ok) {
+          tc_fence_after();
+          for (int h = 0; h < hpi; ++h) qk(h, kslot);
+          umma_commit(&ring_empty[kslot]);
+          if (n_kv == 1) umma_commit(q_empty);
         }
-        umma_commit(pv_done);
-        umma_commit(&kv_empty[s]);
+        for (int j = 0; ok && j < n_kv; ++j) {
+          const uint32_t vslot = C % kRing;
+          if (!wait_or_abort(&ring_full[vslot], (C / kRing) & 1, s_abort)) { ok = false; break; }
+          ++C;
+          for (int h = 0; h < hpi && ok; ++h) {
+            if (!wait_or_abort(&p_full[h], tc & 1, s_abort)) { ok = false; break; }
+            if (j == 0 && qi > 0 && !wait_or_abort(&o_free[h], (qi - 1) & 1, s_abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            pv(h, vslot, j > 0);
+            if (h == 0 && j + 1 < n_kv) {
+              // K_{j+1} for head 0 while head 1's softmax finishes
+              kslot = C % kRing;
+              if (!wait_or_abort(&ring_full[kslot], (C / kRing) & 1, s_abort)) { ok = false; break; }
+              ++C;
+              tc_fence_after();
+              qk(0, kslot);
+            }
+          }
+          if (!ok) break;
+          umma_commit(&ring_empty[vslot]);
+          if (j + 1 < n_kv) {
+            if (hpi == 1 && j + 1 < n_kv) {
+              // one-head items: K_{j+1} was not fetched above
+            }
+            for (int h = 1; h < hpi; ++h) qk(h, kslot);
+            umma_commit(&ring_empty[kslot]);
+            if (j + 2 == n_kv) umma_commit(q_empty);
+          }
+          ++tc;
+        }
+        if (!ok) *s_abort = 1;
+      }
+      __syncwarp();
+      ++qi;
+    }
+  } else {
+    // ---------------------------------------------------- softmax rows ----
+    const int grp = (warp - 2) >> 2;      // which head of the item
+    const int lane_base = 32 * (warp & 3);
+    const int row = lane_base + lane;
+    const uint32_t t_s = tmem + (static_cast<uint32_t>(lane_base) << 16) + grp * kBN;
+    const uint32_t t_o = tmem + (static_cast<uint32_t>(lane_base) << 16) + 256 + grp * kHeadDim;
+    uint8_t* sP = smem + kOffP + grp * kTileBytes;
+    uint32_t tc = 0, qi = 0;
+    const bool active = grp < hpi;
+    for (int item = blockIdx.x; active && item < p.n_items; item += gridDim.x) {
+      if (__any_sync(0xffffffffu, *s_abort != 0)) break;  // warp-uniform exit
+      const int tile = item / items_per_tile;
+      const int head = (item % items_per_tile) * hpi + grp;
+      const int r0 = tile * kBM;
+      int kv_lo, kv_hi;
+      tile_key_range(p, r0, lane, kv_lo, kv_hi);
+      const int n_kv = (kv_hi > kv_lo) ? (kv_hi - kv_lo + kBN - 1) / kBN : 0;
+      const int i = r0 + row;
+      bool valid = false;
+      int start = 0;
+      if (i < p.n_tokens) {
+        const int b = p.batch_idx[i];
+        const int pos = p.input_pos[i];
+        if (b != 0) {
+          valid = true;
+          bool okl = pos >= 0 && pos <= i;
+          if (okl && pos > 0) okl = (p.batch_idx[i - 1] == b) && (p.input_pos[i - 1] == pos - 1);
+          if (!okl && grp == 0) set_dev_err(p.dev_err, PKV_DEV_ERR_LAYOUT);
+          start = (pos >= 0 && pos <= i) ? i - pos : i;
+        }
+      }
+      float m_run = -INFINITY;  // running max, raw score units
+      float l_run = 0.f;
+      bool ok = true;
+      for (int j = 0; j < n_kv && ok; ++j) {
+        // wait outcomes are warp-uniform: the TMEM accesses are warp-collective
+        if (!__all_sync(0xffffffffu, wait_or_abort(&s_full[grp], tc & 1, s_abort))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sr[128];
+        {
+          uint32_t (&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+          uint32_t (&b)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
+          uint32_t (&c)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[64]);
+          uint32_t (&d)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[96]);
+          tmem_ld32(t_s + 0, a);
+          tmem_ld32(t_s + 32, b);
+          tmem_ld32(t_s + 64, c);
+          tmem_ld32(t_s + 96, d);
+          tmem_wait_ld();
+        }
+        // mask: key k = kv_lo + j*128 + c is visible iff start <= k <= i
+        const int k0 = kv_lo + j * kBN;
+        const bool full = valid && k0 >= start && k0 + kBN - 1 <= i;
+        float mx = -INFINITY;
+        if (full) {
+#pragma unroll
+          for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < kBN; ++c) {
+            const int k = k0 + c;
+            const bool vis = valid && k >= start && k <= i;
+            const float v = vis ? __uint_as_float(sr[c]) : -INFINITY;
+            sr[c] = __float_as_uint(v);
+            mx = fmaxf(mx, v);
+          }
+        }
+        const float m_cand = fmaxf(m_run, mx);
+        const bool grow = (m_run == -INFINITY)
+                              ? (m_cand != -INFINITY)
+                              : ((m_cand - m_run) * p.qscale > kRescaleThreshold);
+        const float m_use = grow ? m_cand : m_run;
+        const float alpha = grow ? ex2((m_run - m_use) * p.qscale) : 1.f;  // 0 if m_run=-inf
+        const float neg_m = (m_use == -INFINITY) ? 0.f : -m_use * p.qscale;
+        // P and O of this head are free once its previous PV has completed
+        const bool got = (j == 0) || wait_or_abort(&pv_done[grp], (tc - 1) & 1, s_abort);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float psum = 0.f;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          float e[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float x = __uint_as_float(sr[8 * q + u]);
+            e[u] = (x == -INFINITY) ? 0.f : ex2(fmaf(x, p.qscale, neg_m));
+          }
+          psum += ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+          // 16-byte chunk q of this row (K-major SW128): half q>>3, position (q&7)^(row&7)
+          uint4* dst = reinterpret_cast<uint4*>(sP + (q >> 3) * kHalf + row * 128 +
+                                                (((q & 7) ^ (row & 7)) << 4));
+          *dst = make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
+                            pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
+        }
+        l_run = l_run * alpha + psum;
+        m_run = m_use;
+        if (j > 0 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll
+          for (int c = 0; c < kHeadDim; c += 32) {
+            uint32_t o[32];
+            tmem_ld32(t_o + c, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(t_o + c, o);
+          }
+          tmem_wait_st();
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&p_full[grp]);
+        ++tc;
+      }
+      // ---- epilogue: O / l, LSE ----
+      if (ok && n_kv > 0) {
+        const bool got = wait_or_abort(&pv_done[grp], (tc - 1) & 1, s_abort);
+        if (!__all_sync(0xffffffffu, got)) ok = false;
+      }
+      tc_fence_after();
+      const bool in_range = i < p.n_tokens;
+      const bool has = in_range && valid && ok && l_run > 0.f;
+      const float inv = has ? 1.f / l_run : 0.f;
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
+                            (static_cast<int64_t>(in_range ? i : 0) * p.num_q_heads + head) *
+                                kHeadDim;
+#pragma unroll
+      for (int c = 0; c < kHeadDim; c += 32) {
+        uint32_t o[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0u;
+        if (n_kv > 0 && ok) {  // warp-uniform
+          tmem_ld32(t_o + c, o);
+          tmem_wait_ld();
+        }
+        if (in_range) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 w = make_uint4(0u, 0u, 0u, 0u);
+            if (has) {
+              w.x = pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+            }
+            dst[e / 8] = w;
+          }
+        }
+      }
+      if (in_range)
+        p.lse[static_cast<int64_t>(i) * p.num_q_heads + head] =
+            has ? (m_run * p.qscale + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+      if (n_kv > 0) {
+        tc_fence_before();
+        mbar_arrive(&o_free[grp]);
+        ++qi;
       }
       if (!ok) {
         set_dev_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
         *s_abort = 1;
-      }
-    }
-  } else {
-    // ------------------------------------------------ softmax rows ----
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(lane_base) << 16);
-    float m_run = -INFINITY;  // running max, raw score units
-    float l_run = 0.f;
-    uint8_t* sP = smem + kOffP;
-    bool ok = true;
-    for (int j = 0; j < n_kv && ok; ++j) {
-      // wait outcomes are made warp-uniform: the TMEM accesses below are
-      // warp-collective
-      const bool got_s = mbar_wait_bounded(&s_full[j & 1], (j >> 1) & 1) && !aborted(s_abort);
-      if (!__all_sync(0xffffffffu, got_s)) {
-        ok = false;
         break;
       }
-      tc_fence_after();
-      uint32_t sr[128];
-      {
-        uint32_t (&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
-        uint32_t (&b)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
-        uint32_t (&c)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[64]);
-        uint32_t (&d)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[96]);
-        const uint32_t base = t_lane + static_cast<uint32_t>((j & 1) * kBN);
-        tmem_ld32(base + 0, a);
-        tmem_ld32(base + 32, b);
-        tmem_ld32(base + 64, c);
-        tmem_ld32(base + 96, d);
-        tmem_wait_ld();
-      }
-      // mask: key k = kv_lo + j*128 + c is visible iff start <= k <= i
-      const int k0 = kv_lo + j * kBN;
-      const bool full = valid && k0 >= start && k0 + kBN - 1 <= i;
-      float mx = -INFINITY;
-      if (full) {
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
-      } else {
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-          const int k = k0 + c;
-          const bool vis = valid && k >= start && k <= i;
-          const float v = vis ? __uint_as_float(sr[c]) : -INFINITY;
-          sr[c] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
-        }
-      }
-      // lazy rescale: keep the old max unless it grew by more than 2^8
-      const float m_cand = fmaxf(m_run, mx);
-      const bool grow = (m_run == -INFINITY) ? (m_cand != -INFINITY)
-                                             : ((m_cand - m_run) * p.qscale > kRescaleThreshold);
-      const float m_use = grow ? m_cand : m_run;
-      const float alpha = grow ? exp2f((m_run - m_use) * p.qscale) : 1.f;  // 0 when m_run=-inf
-      const float neg_m = (m_use == -INFINITY) ? 0.f : -m_use * p.qscale;
-      float psum = 0.f;
-      uint32_t pk[64];
-#pragma unroll
-      for (int c = 0; c < kBN; c += 2) {
-        const float x0 = __uint_as_float(sr[c]);
-        const float x1 = __uint_as_float(sr[c + 1]);
-        const float e0 = (x0 == -INFINITY) ? 0.f : exp2f(fmaf(x0, p.qscale, neg_m));
-        const float e1 = (x1 == -INFINITY) ? 0.f : exp2f(fmaf(x1, p.qscale, neg_m));
-        psum += e0 + e1;
-        pk[c >> 1] = pack_bf16x2(e0, e1);
-      }
-      l_run = l_run * alpha + psum;
-      m_run = m_use;
-      // P and O are free once the previous PV product has completed
-      const bool got_pv = (j == 0) || mbar_wait_bounded(pv_done, (j - 1) & 1);
-      if (!__all_sync(0xffffffffu, got_pv)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // P row -> shared memory, K-major SW128: 16-byte chunk q of row r in a
-      // 64-key half lives at chunk position q ^ (r % 8)
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const int half = q >> 3;
-        const int cq = (q & 7) ^ (row & 7);
-        uint4* dst = reinterpret_cast<uint4*>(sP + half * kHalf + row * 128 + cq * 16);
-        *dst = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-      }
-      // O *= alpha when any row of this warp changed its max (warp-collective)
-      if (j > 0 && __any_sync(0xffffffffu, grow)) {
-#pragma unroll
-        for (int c = 0; c < kHeadDim; c += 32) {
-          uint32_t o[32];
-          tmem_ld32(t_lane + kColO + c, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(t_lane + kColO + c, o);
-        }
-        tmem_wait_st();
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(p_full);
     }
-    // ---- epilogue: O / l, LSE ----
-    if (ok && n_kv > 0 && !mbar_wait_bounded(pv_done, (n_kv - 1) & 1)) ok = false;
-    if (!ok) {
-      set_dev_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-      *s_abort = 1;
-    }
-    tc_fence_after();
-    // Every thread of the warp issues the same TMEM loads (they are
-    // warp-collective); only the stores depend on the row.
-    const bool in_range = i < p.n_tokens;
-    const bool has = in_range && valid && ok && l_run > 0.f;
-    const float inv = has ? 1.f / l_run : 0.f;
-    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
-                          (static_cast<int64_t>(in_range ? i : 0) * p.num_q_heads + head) *
-                              kHeadDim;
-#pragma unroll
-    for (int c = 0; c < kHeadDim; c += 32) {
-      uint32_t o[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) o[e] = 0u;
-      if (n_kv > 0) {  // CTA-uniform
-        tmem_ld32(t_lane + kColO + c, o);
-        tmem_wait_ld();
-      }
-      if (in_range) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + c);
-#pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          uint4 w = make_uint4(0u, 0u, 0u, 0u);
-          if (has) {
-            w.x = pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-          }
-          dst[e / 8] = w;
-        }
-      }
-    }
-    if (in_range)
-      p.lse[static_cast<int64_t>(i) * p.num_q_heads + head] =
-          has ? (m_run * p.qscale + log2f(l_run)) * 0.69314718055994531f : -INFINITY;
   }
+  if (*s_abort && threadIdx.x == 0) set_dev_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -453,6 +565,9 @@ pkv_status prefill_entry(const void* q, const void* k, const void* v, int num_q_
       return PKV_ERR_CUDA;
     attr_set[dev] = true;
   }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return PKV_ERR_CUDA;
   PrefillParams prm;
   prm.batch_idx = batch_idx;
   prm.input_pos = input_pos;
@@ -462,11 +577,13 @@ pkv_status prefill_entry(const void* q, const void* k, const void* v, int num_q_
   prm.n_tokens = n_tokens;
   prm.num_q_heads = num_q_heads;
   prm.group = g;
+  prm.heads_per_item = g >= 2 ? 2 : 1;
+  prm.n_tiles = (n_tokens + kBM - 1) / kBM;
+  prm.n_items = prm.n_tiles * (num_q_heads / prm.heads_per_item);
   prm.qscale = scale * 1.4426950408889634f;
-  const int tiles = (n_tokens + kBM - 1) / kBM;
-  const cudaError_t e = launch_kernel(prefill_tcgen05_kernel, dim3(tiles * num_q_heads),
-                                      dim3(kThreads), kSmemBytes, stream, false, qmap, kmap,
-                                      vmap, prm);
+  const int grid = prm.n_items < sms ? prm.n_items : sms;
+  const cudaError_t e = launch_kernel(prefill_tcgen05_kernel, dim3(grid), dim3(kThreads),
+                                      kSmemBytes, stream, false, qmap, kmap, vmap, prm);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

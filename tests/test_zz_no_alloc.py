@@ -55,7 +55,7 @@ def test_static_scratch_matches_workspace_entry_point_twice(maker):
 def test_static_scratch_rejects_batches_past_its_limit():
     case = W.qwen3_b64_decode(0)
     x = _inputs(case)
-    B = 1000   # 8 KV heads x 1000 rows needs about 19 MB, past the built-in 8 MiB
+    B = 500    # 8 KV heads x 500 rows needs about 11 MB, past the built-in 8 MiB
     q = torch.zeros((B, case.num_q_heads, 128), dtype=torch.bfloat16, device="cuda")
     z = torch.zeros(B, dtype=torch.int32, device="cuda")
     with pytest.raises(binding.PkvError) as e:
