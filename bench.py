@@ -405,16 +405,14 @@ def run_pkv(args):
                 "append_gbs": (c.n_tokens * c.num_kv_heads * c.head_dim * 2 * 4)
                 / (app_us * 1e-6) / 1e9}
 
-    case = W.qwen3_b64_decode(0, permute=False)
+    from paged_kv_gqa_pkv_gb300 import sharding
+    # each rank serves its own shard of independent sequences (weak scaling)
+    case = W.qwen3_b64_decode(sharding.shard_seed(rank), permute=False)
     bytes_dec = decode_bytes(case)
     kv_only = int(case.seq_lens.long().sum()) * case.num_kv_heads * case.head_dim * 4
     r = timed_decode(case, args.steps, args.warmup)
-    ms_step = r["total_ms"] / args.steps
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = world * kv_only / (ms_step * 1e-3) / 1e9
+    ms_step = sharding.max_over_ranks(r["total_ms"] / args.steps, device=dev)
+    value = sharding.whole_job_rate(kv_only, world, ms_step * 1e-3) / 1e9
 
     if rank != 0:
         if world > 1:

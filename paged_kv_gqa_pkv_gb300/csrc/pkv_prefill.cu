@@ -83,16 +83,34 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Keys [kv_lo, kv_hi) that rows r0..r0+127 can see: one warp, four rows per
-// lane. Under the packing precondition a valid row i sees [i - pos_i, i].
-__device__ __forceinline__ void tile_key_range(const PrefillParams& p, int r0, int lane,
-                                               int& kv_lo, int& kv_hi) {
+// Keys [kv_lo, kv_hi) that rows r0..r0+127 can see, found by one warp with
+// four rows per lane. Under the packing precondition a valid row i sees
+// [i - pos_i, i]. The loads (TileRaw) are issued one item ahead of their use
+// so their latency hides behind the current item.
+struct TileRaw {
+  int b[4];
+  int pos[4];
+};
+
+__device__ __forceinline__ TileRaw tile_raw_load(const PrefillParams& p, int r0, int lane) {
+  TileRaw t;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const int i = r0 + lane + 32 * m;
+    t.b[m] = (r0 >= 0 && i < p.n_tokens) ? __ldg(p.batch_idx + i) : 0;
+    t.pos[m] = (r0 >= 0 && i < p.n_tokens) ? __ldg(p.input_pos + i) : 0;
+  }
+  return t;
+}
+
+__device__ __forceinline__ void tile_key_range(const TileRaw& t, int r0, int lane, int& kv_lo,
+                                               int& kv_hi) {
   int lo = 0x7fffffff, hi = -1;
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
     const int i = r0 + lane + 32 * m;
-    if (i < p.n_tokens && p.batch_idx[i] != 0) {
-      const int pos = p.input_pos[i];
+    if (t.b[m] != 0) {
+      const int pos = t.pos[m];
       lo = min(lo, (pos >= 0 && pos <= i) ? i - pos : i);
       hi = max(hi, i + 1);
     }
@@ -104,6 +122,29 @@ __device__ __forceinline__ void tile_key_range(const PrefillParams& p, int r0, i
   }
   kv_lo = lo;
   kv_hi = hi;
+}
+
+// This thread's own row of an item: slot/position of the row and of the row
+// before it (for the packing check), loaded one item ahead.
+struct RowRaw {
+  int b, pos, b_prev, pos_prev;
+};
+
+__device__ __forceinline__ RowRaw row_raw_load(const PrefillParams& p, int i) {
+  RowRaw r{0, 0, 0, 0};
+  if (i >= 0 && i < p.n_tokens) {
+    r.b = __ldg(p.batch_idx + i);
+    r.pos = __ldg(p.input_pos + i);
+    if (i > 0) {
+      r.b_prev = __ldg(p.batch_idx + i - 1);
+      r.pos_prev = __ldg(p.input_pos + i - 1);
+    }
+  }
+  return r;
+}
+
+__device__ __forceinline__ int item_r0(const PrefillParams& p, int item, int items_per_tile) {
+  return item < p.n_items ? (item / items_per_tile) * kBM : -1;
 }
 
 // Bounded wait that also gives up when another role has aborted.
@@ -182,13 +223,15 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
     // ---------------------------------------------------- TMA producer ----
     uint32_t L = 0;   // ring loads issued
     uint32_t qi = 0;  // non-empty items
+    TileRaw raw = tile_raw_load(p, item_r0(p, blockIdx.x, items_per_tile), lane);
     for (int item = blockIdx.x; item < p.n_items && !*s_abort; item += gridDim.x) {
       const int tile = item / items_per_tile;
       const int h0 = (item % items_per_tile) * hpi;
       const int kvh = h0 / p.group;
       const int r0 = tile * kBM;
       int kv_lo, kv_hi;
-      tile_key_range(p, r0, lane, kv_lo, kv_hi);
+      tile_key_range(raw, r0, lane, kv_lo, kv_hi);
+      raw = tile_raw_load(p, item_r0(p, item + gridDim.x, items_per_tile), lane);
       if (kv_hi <= kv_lo) continue;
       const int n_kv = (kv_hi - kv_lo + kBN - 1) / kBN;
       if (lane == 0) {
@@ -253,10 +296,12 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
       }
       umma_commit(&pv_done[h]);
     };
+    TileRaw raw = tile_raw_load(p, item_r0(p, blockIdx.x, items_per_tile), lane);
     for (int item = blockIdx.x; item < p.n_items && !*s_abort; item += gridDim.x) {
       const int r0 = (item / items_per_tile) * kBM;
       int kv_lo, kv_hi;
-      tile_key_range(p, r0, lane, kv_lo, kv_hi);
+      tile_key_range(raw, r0, lane, kv_lo, kv_hi);
+      raw = tile_raw_load(p, item_r0(p, item + gridDim.x, items_per_tile), lane);
       if (kv_hi <= kv_lo) continue;
       const int n_kv = (kv_hi - kv_lo + kBN - 1) / kBN;
       if (lane == 0) {
@@ -318,27 +363,32 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
     uint8_t* sP = smem + kOffP + grp * kTileBytes;
     uint32_t tc = 0, qi = 0;
     const bool active = grp < hpi;
+    TileRaw raw = tile_raw_load(p, item_r0(p, blockIdx.x, items_per_tile), lane);
+    const int r0_first = item_r0(p, blockIdx.x, items_per_tile);
+    RowRaw rr = row_raw_load(p, r0_first >= 0 ? r0_first + row : -1);
     for (int item = blockIdx.x; active && item < p.n_items; item += gridDim.x) {
       if (__any_sync(0xffffffffu, *s_abort != 0)) break;  // warp-uniform exit
       const int tile = item / items_per_tile;
       const int head = (item % items_per_tile) * hpi + grp;
       const int r0 = tile * kBM;
       int kv_lo, kv_hi;
-      tile_key_range(p, r0, lane, kv_lo, kv_hi);
+      tile_key_range(raw, r0, lane, kv_lo, kv_hi);
       const int n_kv = (kv_hi > kv_lo) ? (kv_hi - kv_lo + kBN - 1) / kBN : 0;
       const int i = r0 + row;
       bool valid = false;
       int start = 0;
-      if (i < p.n_tokens) {
-        const int b = p.batch_idx[i];
-        const int pos = p.input_pos[i];
-        if (b != 0) {
-          valid = true;
-          bool okl = pos >= 0 && pos <= i;
-          if (okl && pos > 0) okl = (p.batch_idx[i - 1] == b) && (p.input_pos[i - 1] == pos - 1);
-          if (!okl && grp == 0) set_dev_err(p.dev_err, PKV_DEV_ERR_LAYOUT);
-          start = (pos >= 0 && pos <= i) ? i - pos : i;
-        }
+      if (i < p.n_tokens && rr.b != 0) {
+        valid = true;
+        bool okl = rr.pos >= 0 && rr.pos <= i;
+        if (okl && rr.pos > 0) okl = (rr.b_prev == rr.b) && (rr.pos_prev == rr.pos - 1);
+        if (!okl && grp == 0) set_dev_err(p.dev_err, PKV_DEV_ERR_LAYOUT);
+        start = (rr.pos >= 0 && rr.pos <= i) ? i - rr.pos : i;
+      }
+      // next item's metadata, in flight while this item computes
+      {
+        const int r0n = item_r0(p, item + gridDim.x, items_per_tile);
+        raw = tile_raw_load(p, r0n, lane);
+        rr = row_raw_load(p, r0n >= 0 ? r0n + row : -1);
       }
       float m_run = -INFINITY;  // running max, raw score units
       float l_run = 0.f;
@@ -362,22 +412,29 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
           tmem_ld32(t_s + 96, d);
           tmem_wait_ld();
         }
-        // mask: key k = kv_lo + j*128 + c is visible iff start <= k <= i
+        // columns [c_lo, c_hi] of this tile are visible to this row
         const int k0 = kv_lo + j * kBN;
-        const bool full = valid && k0 >= start && k0 + kBN - 1 <= i;
+        const int c_lo = max(start - k0, 0);
+        const int c_hi = min(i - k0, kBN - 1);
+        const bool none = !valid || c_lo > c_hi;
+        const bool full = !none && c_lo == 0 && c_hi == kBN - 1;
         float mx = -INFINITY;
-        if (full) {
+        if (!none) {
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          if (full) {
 #pragma unroll
-          for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
-        } else {
+            for (int c = 0; c < kBN; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sr[c]));
+          } else {
+            const unsigned span = static_cast<unsigned>(c_hi - c_lo);
 #pragma unroll
-          for (int c = 0; c < kBN; ++c) {
-            const int k = k0 + c;
-            const bool vis = valid && k >= start && k <= i;
-            const float v = vis ? __uint_as_float(sr[c]) : -INFINITY;
-            sr[c] = __float_as_uint(v);
-            mx = fmaxf(mx, v);
+            for (int c = 0; c < kBN; ++c) {
+              const bool vis = static_cast<unsigned>(c - c_lo) <= span;
+              const float v = vis ? __uint_as_float(sr[c]) : -INFINITY;
+              sr[c] = __float_as_uint(v);
+              m4[c & 3] = fmaxf(m4[c & 3], v);
+            }
           }
+          mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         }
         const float m_cand = fmaxf(m_run, mx);
         const bool grow = (m_run == -INFINITY)
@@ -394,20 +451,26 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
         }
         tc_fence_after();
         float psum = 0.f;
+        if (none) {
+          // nothing visible: a zero P row (masked keys contribute nothing)
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          float e[8];
+          for (int q = 0; q < 16; ++q)
+            *reinterpret_cast<uint4*>(sP + (q >> 3) * kHalf + row * 128 +
+                                      (((q & 7) ^ (row & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+        } else {
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const float x = __uint_as_float(sr[8 * q + u]);
-            e[u] = (x == -INFINITY) ? 0.f : ex2(fmaf(x, p.qscale, neg_m));
+          for (int q = 0; q < 16; ++q) {
+            float e[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)  // ex2(-inf) = +0 for masked keys
+              e[u] = ex2(fmaf(__uint_as_float(sr[8 * q + u]), p.qscale, neg_m));
+            psum += ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+            // 16-byte chunk q of this row (K-major SW128): half q>>3, position (q&7)^(row&7)
+            *reinterpret_cast<uint4*>(sP + (q >> 3) * kHalf + row * 128 +
+                                      (((q & 7) ^ (row & 7)) << 4)) =
+                make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
+                           pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
           }
-          psum += ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
-          // 16-byte chunk q of this row (K-major SW128): half q>>3, position (q&7)^(row&7)
-          uint4* dst = reinterpret_cast<uint4*>(sP + (q >> 3) * kHalf + row * 128 +
-                                                (((q & 7) ^ (row & 7)) << 4));
-          *dst = make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
-                            pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
         }
         l_run = l_run * alpha + psum;
         m_run = m_use;
