@@ -16,15 +16,19 @@
 // same GQA group, so every K/V tile is loaded once for both heads (a group of
 // one head, G == 1, gives one-head items). Warp roles:
 //  * warp 0 issues TMA: each item's Q tiles, then K and V tiles of 128 keys
-//    into a 3-slot ring of 32 KB half-stages (K_j, V_j, K_j+1, ... in order,
-//    across items), starting at the first key any row of the tile can see;
+//    into a 3-slot ring of 32 KB half-stages, in the MMA thread's order
+//    (K_0, then K_j+1 and V_j for each j, continuing across items), starting
+//    at the first key any row of the tile can see;
 //  * warp 1 (one thread) issues tcgen05 MMAs: S_h = Q_h K^T into TMEM and
-//    O_h += P_h V, interleaved so one head's softmax overlaps the other's MMAs;
+//    O_h += P_h V. The next tile's S_h is computed as soon as the softmax has
+//    read the current S_h into registers (s_free), so QK of tile j+1 runs
+//    while the softmax of tile j computes its exponentials;
 //  * warps 2..5 and 6..9 are the softmax warpgroups of the two heads, one
 //    query row per thread (its TMEM lane): masked online softmax in fp32 with
 //    exp2 and the scale folded in, P written to shared memory as bf16 in the
 //    MMA's K-major 128-byte-swizzled layout, O rescaled in TMEM only when the
-//    running max grows by more than 2^8, and the epilogue O / l -> bf16 + LSE.
+//    running max grows by more than 2^8, and the epilogue O / l -> bf16 + LSE,
+//    staged in the head's P buffer and written with TMA stores.
 // Barrier phases are running counters kept identically by every role.
 // Shared-memory operands (all 128-byte swizzled, 1024-byte aligned atoms):
 // Q, K and P are K-major (64 elements per 128-byte row, two 16 KB halves of
@@ -54,8 +58,8 @@ constexpr int kOffP = kOffQ + 2 * kTileBytes;         // P0, P1
 constexpr int kOffRing = kOffP + 2 * kTileBytes;      // 3 slots
 constexpr int kOffBar = kOffRing + kRing * kTileBytes;
 // q_full, q_empty, ring_full[3], ring_empty[3], s_full[2], p_full[2],
-// pv_done[2], o_free[2]
-constexpr int kNumBars = 16;
+// pv_done[2], o_free[2], s_free[2], grp_sync[2]
+constexpr int kNumBars = 20;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;      // tmem slot, abort flag
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;      // + slack for 1024 alignment
 
@@ -169,7 +173,8 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
                        const __grid_constant__ CUtensorMap kmap,
-                       const __grid_constant__ CUtensorMap vmap, const PrefillParams p) {
+                       const __grid_constant__ CUtensorMap vmap,
+                       const __grid_constant__ CUtensorMap omap, const PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -182,6 +187,8 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
   uint64_t* p_full = bars + 10;     // [2]
   uint64_t* pv_done = bars + 12;    // [2]
   uint64_t* o_free = bars + 14;     // [2]
+  uint64_t* s_free = bars + 16;     // [2]: S_h read into registers, TMEM free
+  uint64_t* grp_sync = bars + 18;   // [2]: barrier of one softmax warpgroup
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
 
@@ -202,6 +209,8 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
       mbar_init(&p_full[h], kGroupThreads);
       mbar_init(&pv_done[h], 1);
       mbar_init(&o_free[h], kGroupThreads);
+      mbar_init(&s_free[h], kGroupThreads);
+      mbar_init(&grp_sync[h], kGroupThreads);
     }
     // After a timeout anywhere in the grid, this CTA does no work (results
     // are unspecified then) instead of waiting out its own limits.
@@ -213,6 +222,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
     tma_prefetch_desc(&qmap);
     tma_prefetch_desc(&kmap);
     tma_prefetch_desc(&vmap);
+    tma_prefetch_desc(&omap);
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
   __syncthreads();
@@ -244,20 +254,23 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
             tma_load_3d(qd + kHalf, &qmap, q_full, 64, h0 + h, r0);
           }
         }
+        // ring order = the MMA thread's consumption order:
+        // K_0, then for each j: K_{j+1} (if any), V_j
+        auto load = [&](const CUtensorMap* map, int j) -> bool {
+          const uint32_t slot = L % kRing;
+          if (L >= kRing && !wait_or_abort(&ring_empty[slot], ((L / kRing) - 1) & 1, s_abort))
+            return false;
+          uint8_t* dst = smem + kOffRing + slot * kTileBytes;
+          mbar_arrive_expect_tx(&ring_full[slot], kTileBytes);
+          tma_load_3d(dst, map, &ring_full[slot], 0, kvh, kv_lo + j * kBN);
+          tma_load_3d(dst + kHalf, map, &ring_full[slot], 64, kvh, kv_lo + j * kBN);
+          ++L;
+          return true;
+        };
+        ok = ok && load(&kmap, 0);
         for (int j = 0; ok && j < n_kv; ++j) {
-          for (int part = 0; part < 2 && ok; ++part) {
-            const uint32_t slot = L % kRing;
-            if (L >= kRing && !wait_or_abort(&ring_empty[slot], ((L / kRing) - 1) & 1, s_abort)) {
-              ok = false;
-              break;
-            }
-            uint8_t* dst = smem + kOffRing + slot * kTileBytes;
-            const CUtensorMap* map = part == 0 ? &kmap : &vmap;
-            mbar_arrive_expect_tx(&ring_full[slot], kTileBytes);
-            tma_load_3d(dst, map, &ring_full[slot], 0, kvh, kv_lo + j * kBN);
-            tma_load_3d(dst + kHalf, map, &ring_full[slot], 64, kvh, kv_lo + j * kBN);
-            ++L;
-          }
+          if (j + 1 < n_kv) ok = load(&kmap, j + 1);
+          ok = ok && load(&vmap, j);
         }
         if (!ok) *s_abort = 1;
       }
@@ -305,17 +318,35 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
       if (kv_hi <= kv_lo) continue;
       const int n_kv = (kv_hi - kv_lo + kBN - 1) / kBN;
       if (lane == 0) {
+        // QK of one tile for every head of the item; S_h must have been read
+        // by the softmax of the previous tile (global tile count t)
+        auto qk_all = [&](uint32_t kslot, uint32_t t) -> bool {
+          for (int h = 0; h < hpi; ++h) {
+            if (t > 0 && !wait_or_abort(&s_free[h], (t - 1) & 1, s_abort)) return false;
+            tc_fence_after();
+            qk(h, kslot);
+          }
+          umma_commit(&ring_empty[kslot]);
+          return true;
+        };
         bool ok = wait_or_abort(q_full, qi & 1, s_abort);
         uint32_t kslot = C % kRing;
         ok = ok && wait_or_abort(&ring_full[kslot], (C / kRing) & 1, s_abort);
         ++C;
         if (ok) {
           tc_fence_after();
-          for (int h = 0; h < hpi; ++h) qk(h, kslot);
-          umma_commit(&ring_empty[kslot]);
-          if (n_kv == 1) umma_commit(q_empty);
+          ok = qk_all(kslot, tc);
+          if (ok && n_kv == 1) umma_commit(q_empty);
         }
         for (int j = 0; ok && j < n_kv; ++j) {
+          if (j + 1 < n_kv) {
+            // K_{j+1}: S of the next tile while this tile's softmax runs
+            kslot = C % kRing;
+            if (!wait_or_abort(&ring_full[kslot], (C / kRing) & 1, s_abort)) { ok = false; break; }
+            ++C;
+            if (!qk_all(kslot, tc + 1)) { ok = false; break; }
+            if (j + 2 == n_kv) umma_commit(q_empty);
+          }
           const uint32_t vslot = C % kRing;
           if (!wait_or_abort(&ring_full[vslot], (C / kRing) & 1, s_abort)) { ok = false; break; }
           ++C;
@@ -327,25 +358,9 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
             }
             tc_fence_after();
             pv(h, vslot, j > 0);
-            if (h == 0 && j + 1 < n_kv) {
-              // K_{j+1} for head 0 while head 1's softmax finishes
-              kslot = C % kRing;
-              if (!wait_or_abort(&ring_full[kslot], (C / kRing) & 1, s_abort)) { ok = false; break; }
-              ++C;
-              tc_fence_after();
-              qk(0, kslot);
-            }
           }
           if (!ok) break;
           umma_commit(&ring_empty[vslot]);
-          if (j + 1 < n_kv) {
-            if (hpi == 1 && j + 1 < n_kv) {
-              // one-head items: K_{j+1} was not fetched above
-            }
-            for (int h = 1; h < hpi; ++h) qk(h, kslot);
-            umma_commit(&ring_empty[kslot]);
-            if (j + 2 == n_kv) umma_commit(q_empty);
-          }
           ++tc;
         }
         if (!ok) *s_abort = 1;
@@ -361,7 +376,15 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
     const uint32_t t_s = tmem + (static_cast<uint32_t>(lane_base) << 16) + grp * kBN;
     const uint32_t t_o = tmem + (static_cast<uint32_t>(lane_base) << 16) + 256 + grp * kHeadDim;
     uint8_t* sP = smem + kOffP + grp * kTileBytes;
-    uint32_t tc = 0, qi = 0;
+    const bool store_thread = (warp & 3) == 2 && lane == 0;  // first warp of the group
+    uint32_t tc = 0, qi = 0, gs = 0;
+    // all 128 threads of this warpgroup; bounded, warp-uniform outcome
+    auto group_sync = [&]() -> bool {
+      mbar_arrive(&grp_sync[grp]);
+      const bool w = wait_or_abort(&grp_sync[grp], gs & 1, s_abort);
+      ++gs;
+      return __all_sync(0xffffffffu, w);
+    };
     const bool active = grp < hpi;
     TileRaw raw = tile_raw_load(p, item_r0(p, blockIdx.x, items_per_tile), lane);
     const int r0_first = item_r0(p, blockIdx.x, items_per_tile);
@@ -412,6 +435,9 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
           tmem_ld32(t_s + 96, d);
           tmem_wait_ld();
         }
+        // S_h is in registers: the next tile's QK may overwrite it
+        tc_fence_before();
+        mbar_arrive(&s_free[grp]);
         // columns [c_lo, c_hi] of this tile are visible to this row
         const int k0 = kv_lo + j * kBN;
         const int c_lo = max(start - k0, 0);
@@ -450,6 +476,14 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
           break;
         }
         tc_fence_after();
+        if (j == 0) {
+          // the previous item's output store may still be reading this buffer
+          if (store_thread) bulk_wait_read_all();
+          if (!group_sync()) {
+            ok = false;
+            break;
+          }
+        }
         float psum = 0.f;
         if (none) {
           // nothing visible: a zero P row (masked keys contribute nothing)
@@ -500,32 +534,50 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
       const bool in_range = i < p.n_tokens;
       const bool has = in_range && valid && ok && l_run > 0.f;
       const float inv = has ? 1.f / l_run : 0.f;
-      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
-                            (static_cast<int64_t>(in_range ? i : 0) * p.num_q_heads + head) *
-                                kHeadDim;
-#pragma unroll
-      for (int c = 0; c < kHeadDim; c += 32) {
-        uint32_t o[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = 0u;
-        if (n_kv > 0 && ok) {  // warp-uniform
-          tmem_ld32(t_o + c, o);
+      if (n_kv > 0 && ok) {
+        // O / l as bf16 into this head's P buffer (same swizzled layout; the
+        // item's last PV has completed), then two TMA stores of 64 head dims
+        // x 128 rows; rows past the end are clipped by the tensor map
+        uint32_t o[128];
+        {
+          uint32_t (&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(&o[0]);
+          uint32_t (&b)[32] = *reinterpret_cast<uint32_t(*)[32]>(&o[32]);
+          uint32_t (&c)[32] = *reinterpret_cast<uint32_t(*)[32]>(&o[64]);
+          uint32_t (&d)[32] = *reinterpret_cast<uint32_t(*)[32]>(&o[96]);
+          tmem_ld32(t_o + 0, a);
+          tmem_ld32(t_o + 32, b);
+          tmem_ld32(t_o + 64, c);
+          tmem_ld32(t_o + 96, d);
           tmem_wait_ld();
         }
-        if (in_range) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c);
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint4 w = make_uint4(0u, 0u, 0u, 0u);
-            if (has) {
-              w.x = pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
-              w.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-              w.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-              w.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-            }
-            dst[e / 8] = w;
+        for (int q = 0; q < 16; ++q) {
+          uint4 w = make_uint4(0u, 0u, 0u, 0u);
+          if (has) {
+            const int e = 8 * q;
+            w.x = pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
           }
+          *reinterpret_cast<uint4*>(sP + (q >> 3) * kHalf + row * 128 +
+                                    (((q & 7) ^ (row & 7)) << 4)) = w;
         }
+        fence_proxy_async_smem();
+        const bool synced = group_sync();
+        if (synced && store_thread) {
+          tma_store_3d(&omap, sP, 0, head, r0);
+          tma_store_3d(&omap, sP + kHalf, 64, head, r0);
+          bulk_commit_group();
+        }
+        if (!synced) ok = false;
+      } else if (in_range) {
+        // no key range at all (padding-only tile) or an aborted item: zeros
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
+                              (static_cast<int64_t>(i) * p.num_q_heads + head) * kHeadDim;
+#pragma unroll
+        for (int c = 0; c < kHeadDim; c += 8)
+          *reinterpret_cast<uint4*>(orow + c) = make_uint4(0u, 0u, 0u, 0u);
       }
       if (in_range)
         p.lse[static_cast<int64_t>(i) * p.num_q_heads + head] =
@@ -542,6 +594,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
       }
     }
   }
+  if (warp >= 2 && (warp & 3) == 2 && lane == 0) bulk_wait_all();  // output stores done
   if (*s_abort && threadIdx.x == 0) set_dev_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
   tc_fence_before();
   __syncthreads();
@@ -614,10 +667,11 @@ pkv_status prefill_entry(const void* q, const void* k, const void* v, int num_q_
   if (static_cast<long long>(((n_tokens + kBM - 1) / kBM)) * num_q_heads > INT32_MAX)
     return PKV_ERR_ARG;
 
-  CUtensorMap qmap, kmap, vmap;
+  CUtensorMap qmap, kmap, vmap, omap;
   if (!encode_packed_map(&qmap, q, num_q_heads, n_tokens) ||
       !encode_packed_map(&kmap, k, num_kv_heads, n_tokens) ||
-      !encode_packed_map(&vmap, v, num_kv_heads, n_tokens))
+      !encode_packed_map(&vmap, v, num_kv_heads, n_tokens) ||
+      !encode_packed_map(&omap, out, num_q_heads, n_tokens))
     return PKV_ERR_ARG;
 
   static bool attr_set[64] = {};
@@ -646,7 +700,7 @@ pkv_status prefill_entry(const void* q, const void* k, const void* v, int num_q_
   prm.qscale = scale * 1.4426950408889634f;
   const int grid = prm.n_items < sms ? prm.n_items : sms;
   const cudaError_t e = launch_kernel(prefill_tcgen05_kernel, dim3(grid), dim3(kThreads),
-                                      kSmemBytes, stream, false, qmap, kmap, vmap, prm);
+                                      kSmemBytes, stream, false, qmap, kmap, vmap, omap, prm);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
