@@ -51,6 +51,21 @@ def _peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def captured_traffic(key: str):
+    """DRAM bytes per call from the committed ncu capture (profiles/traffic.json),
+    or None when the kernel source has changed since that capture."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[key]
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != rec["source_sha256"]:
+                return None
+        return int(rec["dram_bytes_per_call"])
+    except Exception:
+        return None
+
+
 def decode_bytes(case) -> int:
     """Algorithmic bytes of one decode launch: K and V rows of every attended
     key (all kv heads), q in, out and lse out, the page-table entries walked,
@@ -401,6 +416,7 @@ def run_pkv(args):
                 "attention_call_us": att_us, "algorithmic_flops": flops,
                 "tflops": tf, "bound": "tensor", "peak_tflops": bf16_peak,
                 "frac": tf / bf16_peak, "peak_kind": peak_kind,
+                "traffic": captured_traffic("prefill_call"),
                 "append_call_us": app_us,
                 "append_gbs": (c.n_tokens * c.num_kv_heads * c.head_dim * 2 * 4)
                 / (app_us * 1e-6) / 1e9}
@@ -440,7 +456,8 @@ def run_pkv(args):
         "timing": f"CUDA-graph replay of {r['per_graph']}-step graphs; decode call = replay "
                   f"of {r['per_graph']} decode calls / {r['per_graph']}",
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None,
+                     "frac": achieved / hbm_peak, "traffic": captured_traffic("decode_call"),
+                     "traffic_unit": "bytes per decode call (ncu dram read+write)",
                      "kernel": "pkv_decode_attention (split-KV pass + LSE merge)",
                      "peak_kind": peak_kind, "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS},
         "permuted_pages": {"decode_call_us": rp["dec_ms"] * 1e3,
