@@ -69,12 +69,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 thread_local cudaError_t t_last_cuda_error = cudaSuccess;
 
-// Records a failed runtime call for pkv_last_cuda_error_string().
-pkv_status cuda_status(cudaError_t e) {
-  if (e == cudaSuccess) return PKV_OK;
-  t_last_cuda_error = e;
-  return PKV_ERR_CUDA;
-}
+pkv_status cuda_status(cudaError_t e) { return pkv::record_cuda_status(e); }
 
 pkv_status check_cache(const pkv_cache_desc* c) {
   if (c == nullptr) return PKV_ERR_ARG;
@@ -115,6 +110,14 @@ pkv_status encode_pool_map(CUtensorMap* map, const void* pool, const pkv_cache_d
 }
 
 }  // namespace
+
+namespace pkv {
+pkv_status record_cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return PKV_OK;
+  t_last_cuda_error = e;
+  return PKV_ERR_CUDA;
+}
+}  // namespace pkv
 
 extern "C" {
 

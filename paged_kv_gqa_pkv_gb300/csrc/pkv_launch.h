@@ -68,6 +68,10 @@ int decode_workers_for_device(int sm_count);
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 
+// PKV_OK for cudaSuccess; otherwise remembers `e` for
+// pkv_last_cuda_error_string() and returns PKV_ERR_CUDA.
+pkv_status record_cuda_status(cudaError_t e);
+
 // Validation and launch of pkv_prefill_attention (pkv_prefill.cu).
 pkv_status prefill_entry(const void* q, const void* k, const void* v, int num_q_heads,
                          int num_kv_heads, int head_dim, const int32_t* batch_idx,

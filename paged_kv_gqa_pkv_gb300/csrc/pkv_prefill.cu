@@ -170,6 +170,8 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
 
 }  // namespace
 
+// 10 warps: two of the four SM sub-partitions hold three warps, so at most
+// 16384 / 96 = 170 registers per thread (ptxas settles on 168)
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
                        const __grid_constant__ CUtensorMap kmap,
@@ -677,9 +679,9 @@ pkv_status prefill_entry(const void* q, const void* k, const void* v, int num_q_
   static bool attr_set[64] = {};
   if (dev < 0 || dev >= 64) return PKV_ERR_DEVICE;
   if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(prefill_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
-      return PKV_ERR_CUDA;
+    const cudaError_t ea = cudaFuncSetAttribute(
+        prefill_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (ea != cudaSuccess) return record_cuda_status(ea);
     attr_set[dev] = true;
   }
   int sms = 0;
@@ -701,7 +703,7 @@ pkv_status prefill_entry(const void* q, const void* k, const void* v, int num_q_
   const int grid = prm.n_items < sms ? prm.n_items : sms;
   const cudaError_t e = launch_kernel(prefill_tcgen05_kernel, dim3(grid), dim3(kThreads),
                                       kSmemBytes, stream, false, qmap, kmap, vmap, omap, prm);
-  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return record_cuda_status(e);
 }
 
 }  // namespace pkv
