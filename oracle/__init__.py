@@ -16,6 +16,8 @@ from .paged_attention import (  # noqa: F401
     f64_to_bf16_bits,
     physical_slot,
     append,
+    rope,
+    append_rope,
     gather_logical,
     attend,
     decode_attention,

@@ -147,6 +147,51 @@ def append(k_pool: np.ndarray, v_pool: np.ndarray, page_table: np.ndarray,
     return k_out, v_out, bad
 
 
+def rope(x: np.ndarray, positions: np.ndarray, cos_table: np.ndarray,
+         sin_table: np.ndarray) -> np.ndarray:
+    """Rotary position embedding in the rotate-half form the pages apply to q
+    and k before the cache write ("qwen3_flex_inference.py", ``_apply_rotary``:
+    ``x * cos + rotate_half(x) * sin`` with ``rotate_half(x) = cat(-x2, x1)``).
+
+    ``x`` is bf16 bits ``[N, H, D]``; token i uses row ``positions[i]`` of the
+    tables ``cos_table``/``sin_table`` (``[L, D/2]``, the half-width table: the
+    full-width cos/sin repeat it for the second half). For each head, with
+    ``x1 = x[:D/2]``, ``x2 = x[D/2:]``, ``c = cos[p]``, ``s = sin[p]``:
+    ``out1 = x1*c - x2*s`` and ``out2 = x2*c + x1*s``. Returns float64.
+    """
+    xf = bf16_bits_to_f64(x)
+    half = xf.shape[-1] // 2
+    c = np.asarray(cos_table, dtype=np.float64)[np.asarray(positions, dtype=np.int64)]
+    s = np.asarray(sin_table, dtype=np.float64)[np.asarray(positions, dtype=np.int64)]
+    c = c[:, None, :]
+    s = s[:, None, :]
+    x1, x2 = xf[..., :half], xf[..., half:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+def append_rope(k_pool: np.ndarray, v_pool: np.ndarray, page_table: np.ndarray,
+                k_new: np.ndarray, v_new: np.ndarray, batch_idx: np.ndarray,
+                input_pos: np.ndarray, page_size: int, cos_table: np.ndarray,
+                sin_table: np.ndarray):
+    """KV append with the rotary embedding applied to K first: K rows are
+    ``rope(k_new)`` rounded to bf16 (nearest even), V rows are copied as
+    they are. A token whose position has no table row is reported and not
+    written. Returns ``(k_pool_out, v_pool_out, bad_tokens)``."""
+    n = len(batch_idx)
+    pos = np.asarray(input_pos, dtype=np.int64)
+    in_table = (pos >= 0) & (pos < len(cos_table))
+    k_rot = np.array(k_new, dtype=np.uint16, copy=True)
+    if in_table.any():
+        k_rot[in_table] = f64_to_bf16_bits(
+            rope(k_new[in_table], pos[in_table], cos_table, sin_table))
+    keep = [i for i in range(n) if in_table[i] or int(batch_idx[i]) == 0]
+    k_out, v_out, bad = append(k_pool, v_pool, page_table, k_rot[keep], v_new[keep],
+                               np.asarray(batch_idx)[keep], pos[keep], page_size)
+    bad = sorted([keep[i] for i in bad] +
+                 [i for i in range(n) if not in_table[i] and int(batch_idx[i]) != 0])
+    return k_out, v_out, bad
+
+
 # --------------------------------------------------------------------------
 # Attention
 # --------------------------------------------------------------------------

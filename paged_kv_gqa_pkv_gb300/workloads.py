@@ -266,6 +266,17 @@ def packed_prefill(seed: int = 0, n_docs: int = 64, lo: int = 64,
         info={"tokens": T, "pairs": int(sum(n * (n + 1) // 2 for n in doc_lens))})
 
 
+def rope_tables(max_pos: int, head_dim: int = HEAD_DIM, theta: float = 1.0e6):
+    """fp32 cos/sin tables ``[max_pos, head_dim/2]`` of the standard rotary
+    embedding: angle ``p * theta**(-2i/head_dim)`` for row p, column i
+    (Qwen3's ``rope_theta`` is 1e6). These are inputs to the RoPE-fused
+    append, the way the model passes cos/sin to its attention layers."""
+    i = torch.arange(0, head_dim // 2, dtype=torch.float64)
+    inv_freq = theta ** (-2.0 * i / head_dim)
+    ang = torch.arange(max_pos, dtype=torch.float64)[:, None] * inv_freq[None, :]
+    return torch.cos(ang).to(torch.float32), torch.sin(ang).to(torch.float32)
+
+
 WORKLOADS = {
     "tiny_decode": tiny_decode,
     "qwen3_b64_decode": qwen3_b64_decode,

@@ -397,3 +397,69 @@ ALL_CHECKS = [
     check_prefill_interleaved_documents,
     check_prefill_decode_consistency,
 ]
+
+
+# ---------------------------------------------------------------- rope ----
+
+def check_rope_closed_forms(orc):
+    gen = torch.Generator().manual_seed(47)
+    N, H = 6, 3
+    x = _bits(_rand_bf16(gen, (N, H, D)))
+    xf = orc.bf16_bits_to_f64(x)
+    half = D // 2
+    pos = np.arange(N)
+    # angle 0: identity
+    c0, s0 = np.ones((N, half)), np.zeros((N, half))
+    assert np.array_equal(orc.rope(x, pos, c0, s0), xf)
+    # angle 90 degrees: (x1, x2) -> (-x2, x1)
+    c9, s9 = np.zeros((N, half)), np.ones((N, half))
+    r = orc.rope(x, pos, c9, s9)
+    assert np.array_equal(r[..., :half], -xf[..., half:]) and np.array_equal(r[..., half:], xf[..., :half])
+    # a rotation keeps each (d, d + D/2) pair's length, for any angles
+    ang = np.random.default_rng(1).uniform(-7, 7, (N, half))
+    r = orc.rope(x, pos, np.cos(ang), np.sin(ang))
+    n_in = xf[..., :half] ** 2 + xf[..., half:] ** 2
+    n_out = r[..., :half] ** 2 + r[..., half:] ** 2
+    assert np.allclose(n_in, n_out, rtol=1e-12, atol=1e-12)
+
+
+def check_rope_relative_position(orc):
+    """With the standard table, <rope(q, m), rope(k, n)> depends only on m - n."""
+    from paged_kv_gqa_pkv_gb300.workloads import rope_tables
+    cos_t, sin_t = rope_tables(64)
+    gen = torch.Generator().manual_seed(53)
+    q = _bits(_rand_bf16(gen, (1, 1, D)))
+    k = _bits(_rand_bf16(gen, (1, 1, D)))
+    def dot(m, n):
+        return float(np.sum(orc.rope(q, np.array([m]), cos_t.numpy(), sin_t.numpy()) *
+                            orc.rope(k, np.array([n]), cos_t.numpy(), sin_t.numpy())))
+    for m, n in [(9, 4), (30, 2), (17, 17)]:
+        assert abs(dot(m, n) - dot(m + 13, n + 13)) < 1e-5 * (1 + abs(dot(m, n)))
+    assert abs(dot(9, 4) - dot(4, 9)) > 1e-3   # but it does depend on the sign of m - n
+
+
+def check_append_rope(orc):
+    gen = torch.Generator().manual_seed(59)
+    ps, P, hkv = 16, 10, 2
+    from paged_kv_gqa_pkv_gb300.workloads import rope_tables
+    cos_t, sin_t = rope_tables(40)
+    kp = _bits(_rand_bf16(gen, (P * ps, hkv, D)))
+    vp = _bits(_rand_bf16(gen, (P * ps, hkv, D)))
+    table = np.full((3, 4), -1, dtype=np.int32)
+    table[1, :2] = [3, 5]
+    table[2, :3] = [7, 1, 2]
+    bidx = np.array([1, 2, 0, 2, 1], dtype=np.int32)
+    pos = np.array([0, 33, 3, 39, 40], dtype=np.int32)   # 40: past the table
+    kn = _bits(_rand_bf16(gen, (5, hkv, D)))
+    vn = _bits(_rand_bf16(gen, (5, hkv, D)))
+    ko, vo, bad = orc.append_rope(kp, vp, table, kn, vn, bidx, pos, ps, cos_t.numpy(),
+                                  sin_t.numpy())
+    assert bad == [4]
+    # position 0 is the identity rotation: the raw row lands unchanged
+    assert np.array_equal(ko[3 * ps + 0], kn[0])
+    rot = orc.f64_to_bf16_bits(orc.rope(kn[1:2], pos[1:2], cos_t.numpy(), sin_t.numpy()))[0]
+    assert np.array_equal(ko[2 * ps + 33 % ps], rot) and np.array_equal(vo[2 * ps + 1], vn[1])
+    assert not np.array_equal(rot, kn[1])
+
+
+ALL_CHECKS += [check_rope_closed_forms, check_rope_relative_position, check_append_rope]

@@ -151,7 +151,41 @@ def _round_via_f32(x):
     return t.view(torch.int16).numpy().view(np.uint16)
 
 
+def _rope_sign_flipped(x, positions, cos_table, sin_table):
+    xf = orc.bf16_bits_to_f64(x)
+    half = xf.shape[-1] // 2
+    c = np.asarray(cos_table, dtype=np.float64)[np.asarray(positions)][:, None, :]
+    s_ = np.asarray(sin_table, dtype=np.float64)[np.asarray(positions)][:, None, :]
+    x1, x2 = xf[..., :half], xf[..., half:]
+    return np.concatenate([x1 * c + x2 * s_, x2 * c - x1 * s_], axis=-1)   # planted: sign
+
+
+def _rope_interleaved(x, positions, cos_table, sin_table):
+    xf = orc.bf16_bits_to_f64(x)
+    c = np.asarray(cos_table, dtype=np.float64)[np.asarray(positions)][:, None, :]
+    s_ = np.asarray(sin_table, dtype=np.float64)[np.asarray(positions)][:, None, :]
+    x1, x2 = xf[..., 0::2], xf[..., 1::2]          # planted: pairs (2i, 2i+1)
+    out = np.empty_like(xf)
+    out[..., 0::2] = x1 * c - x2 * s_
+    out[..., 1::2] = x2 * c + x1 * s_
+    return out
+
+
+_real_append_rope = orc.append_rope
+
+
+def _append_rope_on_v(k_pool, v_pool, table, k_new, v_new, bidx, pos, ps, cos_t, sin_t):
+    # planted: the rotation is applied to V as well
+    ok = (np.asarray(pos) >= 0) & (np.asarray(pos) < len(cos_t))
+    v_rot = np.array(v_new, copy=True)
+    v_rot[ok] = orc.f64_to_bf16_bits(orc.rope(v_new[ok], np.asarray(pos)[ok], cos_t, sin_t))
+    return _real_append_rope(k_pool, v_pool, table, k_new, v_rot, bidx, pos, ps, cos_t, sin_t)
+
+
 MUTANTS.update({
+    "rope_sign_flipped": ("rope", _rope_sign_flipped),
+    "rope_interleaved_pairs": ("rope", _rope_interleaved),
+    "append_rope_rotates_v": ("append_rope", _append_rope_on_v),
     "page_formula_swapped": ("physical_slot", _physical_slot_swapped),
     "unreserved_page_accepted": ("physical_slot", _physical_slot_no_range_check),
     "append_writes_padding_slot": ("append", _append_writes_padding),
