@@ -14,6 +14,7 @@
  * ("qwen3_flex_inference.py", attention forward, _decode_step_eager,
  * _prefill):
  *   pkv_append            - write new tokens' K/V rows through the page table
+ *   pkv_append_rope       - the same with the rotary embedding applied to K
  *   pkv_decode_attention  - one query token per row, GQA, over the pages
  *   pkv_prefill_attention - packed document-causal attention over fresh k/v
  *
@@ -97,6 +98,29 @@ pkv_status pkv_append(const pkv_cache_desc* cache, void* k_pool, void* v_pool,
                       const void* v_new, const int32_t* batch_idx,
                       const int32_t* input_pos, int n_tokens, int32_t* dev_err,
                       cudaStream_t stream);
+
+/*
+ * pkv_append_rope - pkv_append with the rotary position embedding applied to
+ * each new K row on the way into the pool (V rows are copied unchanged).
+ * Source: "qwen3_flex_inference.py", _apply_rotary (x * cos + rotate_half(x)
+ * * sin with rotate_half(x) = cat(-x2, x1), applied to k right before the
+ * cache write in the attention forward).
+ *
+ * rope_cos, rope_sin: fp32 [rope_len, D/2] row-major, 16-byte aligned; row p
+ * holds the cos/sin of the angles of position p (the full-width tables repeat
+ * them for the second half of D). For each kv head of token i at position
+ * p = input_pos[i], with x1 = k_new[i][h][0:D/2], x2 = k_new[i][h][D/2:D],
+ * c = rope_cos[p], s = rope_sin[p]:
+ *     K row = bf16_rne(concat(x1*c - x2*s, x2*c + x1*s))   (computed in fp32)
+ * A position outside [0, rope_len) sets PKV_DEV_ERR_BAD_POS and skips the
+ * token; everything else (slots, pages, errors, races) is as pkv_append.
+ */
+pkv_status pkv_append_rope(const pkv_cache_desc* cache, void* k_pool, void* v_pool,
+                           const int32_t* page_table, const void* k_new,
+                           const void* v_new, const int32_t* batch_idx,
+                           const int32_t* input_pos, int n_tokens,
+                           const float* rope_cos, const float* rope_sin, int rope_len,
+                           int32_t* dev_err, cudaStream_t stream);
 
 /*
  * pkv_decode_workspace_size - bytes of workspace pkv_decode_attention needs

@@ -30,7 +30,7 @@ DEV_ERR_BAD_POS = 0x4
 DEV_ERR_LAYOUT = 0x8
 DEV_ERR_TIMEOUT = 0x10
 
-EXPORTED = ("pkv_append", "pkv_decode_workspace_size", "pkv_decode_attention",
+EXPORTED = ("pkv_append", "pkv_append_rope", "pkv_decode_workspace_size", "pkv_decode_attention",
             "pkv_prefill_attention", "pkv_status_string",
             "pkv_status_from_device_error", "pkv_last_cuda_error_string")
 
@@ -69,6 +69,9 @@ def load_library() -> ctypes.CDLL:
     desc_p = ctypes.POINTER(CacheDesc)
     lib.pkv_append.argtypes = [desc_p, vp, vp, i32p, vp, vp, i32p, i32p, c_int, i32p, vp]
     lib.pkv_append.restype = c_int
+    lib.pkv_append_rope.argtypes = [desc_p, vp, vp, i32p, vp, vp, i32p, i32p, c_int, f32p, f32p,
+                                    c_int, i32p, vp]
+    lib.pkv_append_rope.restype = c_int
     lib.pkv_decode_workspace_size.argtypes = [desc_p, c_int, c_int, c_int]
     lib.pkv_decode_workspace_size.restype = c_size
     lib.pkv_decode_attention.argtypes = [desc_p, vp, vp, i32p, vp, c_int, i32p, i32p, c_int,
@@ -146,6 +149,30 @@ def pkv_append(k_pool, v_pool, page_table, k_new, v_new, batch_idx, input_pos,
         _ptr(v_new), _ptr(batch_idx), _ptr(input_pos), int(batch_idx.numel()),
         _ptr(dev_err), _stream(stream))
     _check("pkv_append", st)
+
+
+def pkv_append_rope(k_pool, v_pool, page_table, k_new, v_new, batch_idx, input_pos,
+                    page_size: int, rope_cos, rope_sin, dev_err=None, stream=None) -> None:
+    """pkv_append with the rotary embedding applied to K; rope_cos/rope_sin are
+    fp32 [L, D/2] tables indexed by position."""
+    for name, t, dt, nd in (("k_pool", k_pool, torch.bfloat16, 3),
+                            ("v_pool", v_pool, torch.bfloat16, 3),
+                            ("page_table", page_table, torch.int32, 2),
+                            ("k_new", k_new, torch.bfloat16, 3),
+                            ("v_new", v_new, torch.bfloat16, 3),
+                            ("batch_idx", batch_idx, torch.int32, 1),
+                            ("input_pos", input_pos, torch.int32, 1),
+                            ("rope_cos", rope_cos, torch.float32, 2),
+                            ("rope_sin", rope_sin, torch.float32, 2)):
+        _need(t, name, dt, nd)
+    if rope_cos.shape != rope_sin.shape or rope_cos.shape[1] * 2 != k_new.shape[2]:
+        raise ValueError("rope tables must both be [L, D/2]")
+    desc = cache_desc(k_pool, page_table, page_size)
+    st = load_library().pkv_append_rope(
+        ctypes.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(k_new),
+        _ptr(v_new), _ptr(batch_idx), _ptr(input_pos), int(batch_idx.numel()), _ptr(rope_cos),
+        _ptr(rope_sin), int(rope_cos.shape[0]), _ptr(dev_err), _stream(stream))
+    _check("pkv_append_rope", st)
 
 
 def pkv_decode_workspace_size(k_pool, page_table, page_size: int, batch: int,

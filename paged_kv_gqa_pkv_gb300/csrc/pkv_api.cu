@@ -180,6 +180,47 @@ pkv_status pkv_append(const pkv_cache_desc* cache, void* k_pool, void* v_pool,
   return cuda_status(pkv::launch_append(p, stream));
 }
 
+pkv_status pkv_append_rope(const pkv_cache_desc* cache, void* k_pool, void* v_pool,
+                           const int32_t* page_table, const void* k_new, const void* v_new,
+                           const int32_t* batch_idx, const int32_t* input_pos, int n_tokens,
+                           const float* rope_cos, const float* rope_sin, int rope_len,
+                           int32_t* dev_err, cudaStream_t stream) {
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (n_tokens < 0 || rope_len <= 0) return PKV_ERR_ARG;
+  if (n_tokens == 0) return PKV_OK;
+  if (!k_pool || !v_pool || !page_table || !k_new || !v_new || !batch_idx || !input_pos ||
+      !rope_cos || !rope_sin)
+    return PKV_ERR_ARG;
+  if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) ||
+      !aligned(rope_cos, 16) || !aligned(rope_sin, 16) || !aligned(page_table, 4) ||
+      !aligned(batch_idx, 4) || !aligned(input_pos, 4) || !aligned(dev_err, 4))
+    return PKV_ERR_ALIGN;
+  int sms = 0;
+  st = device_info(&sms);
+  if (st != PKV_OK) return st;
+  pkv::AppendRopeParams p;
+  p.a.k_pool = k_pool;
+  p.a.v_pool = v_pool;
+  p.a.page_table = page_table;
+  p.a.k_new = k_new;
+  p.a.v_new = v_new;
+  p.a.batch_idx = batch_idx;
+  p.a.input_pos = input_pos;
+  p.a.dev_err = dev_err;
+  p.a.n_tokens = n_tokens;
+  p.a.row_vecs = cache->num_kv_heads * cache->head_dim * 2 / 16;
+  p.a.page_size = cache->page_size;
+  p.a.num_pages = cache->num_pages;
+  p.a.max_batch = cache->max_batch;
+  p.a.max_blocks = cache->max_blocks;
+  p.rope_cos = rope_cos;
+  p.rope_sin = rope_sin;
+  p.rope_len = rope_len;
+  p.num_kv_heads = cache->num_kv_heads;
+  return cuda_status(pkv::launch_append_rope(p, stream));
+}
+
 size_t pkv_decode_workspace_size(const pkv_cache_desc* cache, int batch, int num_q_heads,
                                  int max_seq_len) {
   (void)max_seq_len;

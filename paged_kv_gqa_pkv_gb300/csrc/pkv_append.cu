@@ -57,6 +57,95 @@ append_kernel(AppendParams p) {
   }
 }
 
+// The same append with the rotary embedding fused in front of the K write
+// ("qwen3_flex_inference.py", _apply_rotary, applied to k right before the
+// cache update): for each head, dims d and d + D/2 form a pair rotated by the
+// angle of (position, d): out_d = k_d c - k_{d+D/2} s, out_{d+D/2} =
+// k_{d+D/2} c + k_d s, computed in fp32 and rounded to bf16 (nearest even).
+// A lane takes one 16-byte chunk of the first half of a head and its partner
+// chunk of the second half; the tables' eight cos and sin values of that
+// chunk are two float4 loads each. V rows are copied unchanged.
+// a*c - b*s and a*c + b*s accurate to about one fp32 ulp of the result even
+// when the two products nearly cancel: the rounding error of b*s is kept
+// exactly (an FMA) and folded back in after the fused multiply-add.
+__device__ __forceinline__ float rot_diff(float a, float c, float b, float s) {
+  const float p = b * s;
+  const float e = fmaf(b, s, -p);
+  return fmaf(a, c, -p) - e;
+}
+__device__ __forceinline__ float rot_sum(float a, float c, float b, float s) {
+  const float p = b * s;
+  const float e = fmaf(b, s, -p);
+  return fmaf(a, c, p) + e;
+}
+
+__global__ void __launch_bounds__(kAppendWarps * 32)
+append_rope_kernel(AppendRopeParams rp) {
+  pdl_wait_primary();
+  pdl_launch_dependents();
+  const AppendParams& p = rp.a;
+  const int lane = threadIdx.x & 31;
+  const int i = blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
+  if (i >= p.n_tokens) return;
+
+  const int b = p.batch_idx[i];
+  const int pos = p.input_pos[i];
+  if (b == 0) return;  // padding slot: no-op
+  int err = 0;
+  if (b < 0 || b >= p.max_batch) err |= PKV_DEV_ERR_BAD_SLOT;
+  const int block = pos / p.page_size;
+  if (pos < 0 || block >= p.max_blocks || pos >= rp.rope_len) err |= PKV_DEV_ERR_BAD_POS;
+  int page = -1;
+  if (!err) {
+    page = p.page_table[static_cast<int64_t>(b) * p.max_blocks + block];
+    if (page < 0 || page >= p.num_pages) err |= PKV_DEV_ERR_BAD_PAGE;
+  }
+  if (err) {
+    if (lane == 0) set_dev_err(p.dev_err, err);
+    return;
+  }
+  const int64_t row = static_cast<int64_t>(page) * p.page_size + pos % p.page_size;
+  const int vecs = p.row_vecs;
+  const uint4* ks = reinterpret_cast<const uint4*>(p.k_new) + static_cast<int64_t>(i) * vecs;
+  const uint4* vs = reinterpret_cast<const uint4*>(p.v_new) + static_cast<int64_t>(i) * vecs;
+  uint4* kd = reinterpret_cast<uint4*>(p.k_pool) + row * vecs;
+  uint4* vd = reinterpret_cast<uint4*>(p.v_pool) + row * vecs;
+  for (int e = lane; e < vecs; e += 32) vd[e] = __ldg(vs + e);
+
+  const float4* cs = reinterpret_cast<const float4*>(rp.rope_cos + static_cast<int64_t>(pos) * (kHeadDim / 2));
+  const float4* sn = reinterpret_cast<const float4*>(rp.rope_sin + static_cast<int64_t>(pos) * (kHeadDim / 2));
+  const int pairs = rp.num_kv_heads * 8;  // eight 16-byte chunk pairs per head
+  for (int e = lane; e < pairs; e += 32) {
+    const int h = e >> 3;
+    const int c = e & 7;
+    const uint4 a = __ldg(ks + h * 16 + c);
+    const uint4 bb = __ldg(ks + h * 16 + 8 + c);
+    const float4 c0 = __ldg(cs + 2 * c), c1 = __ldg(cs + 2 * c + 1);
+    const float4 s0 = __ldg(sn + 2 * c), s1 = __ldg(sn + 2 * c + 1);
+    const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+    const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
+    uint32_t o1[4], o2[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float x1l = bf16lo(aw[u]), x1h = bf16hi(aw[u]);
+      const float x2l = bf16lo(bw[u]), x2h = bf16hi(bw[u]);
+      const float cl = cv[2 * u], ch = cv[2 * u + 1], sl = sv[2 * u], sh = sv[2 * u + 1];
+      o1[u] = pack_bf16x2(rot_diff(x1l, cl, x2l, sl), rot_diff(x1h, ch, x2h, sh));
+      o2[u] = pack_bf16x2(rot_sum(x2l, cl, x1l, sl), rot_sum(x2h, ch, x1h, sh));
+    }
+    kd[h * 16 + c] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+    kd[h * 16 + 8 + c] = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+  }
+}
+
+cudaError_t launch_append_rope(const AppendRopeParams& p, cudaStream_t stream) {
+  const int grid = (p.a.n_tokens + kAppendWarps - 1) / kAppendWarps;
+  return launch_kernel(append_rope_kernel, dim3(grid), dim3(kAppendWarps * 32), 0, stream,
+                       /*programmatic=*/true, p);
+}
+
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
   const int grid = (p.n_tokens + kAppendWarps - 1) / kAppendWarps;
   return launch_kernel(append_kernel, dim3(grid), dim3(kAppendWarps * 32), 0, stream,

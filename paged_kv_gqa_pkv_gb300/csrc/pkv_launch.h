@@ -12,6 +12,9 @@
 
 namespace pkv {
 
+struct AppendParams;
+struct AppendRopeParams;
+
 struct AppendParams {
   void* k_pool;
   void* v_pool;
@@ -27,6 +30,15 @@ struct AppendParams {
   int num_pages;
   int max_batch;
   int max_blocks;
+};
+
+// Append with the rotary embedding applied to K (tables fp32 [rope_len, D/2]).
+struct AppendRopeParams {
+  AppendParams a;
+  const float* rope_cos;
+  const float* rope_sin;
+  int rope_len;
+  int num_kv_heads;
 };
 
 // Split-KV decode. The work of a call is the sequence of 16-token tiles of all
@@ -67,6 +79,7 @@ size_t decode_workspace_bytes(int batch, int num_kv_heads, int group, int num_wo
 int decode_workers_for_device(int sm_count);
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_append_rope(const AppendRopeParams& p, cudaStream_t stream);
 
 // PKV_OK for cudaSuccess; otherwise remembers `e` for
 // pkv_last_cuda_error_string() and returns PKV_ERR_CUDA.

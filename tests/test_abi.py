@@ -116,3 +116,15 @@ def test_without_a_gpu_calls_fail_cleanly(lib):
     st = lib.pkv_append(ctypes.byref(d), P(256), P(256), P(256), P(256), P(256), P(256),
                         P(256), 4, None, None)
     assert st in (5, 6)
+
+
+def test_append_rope_rejects_bad_arguments(lib):
+    d = _desc()
+    args = lambda cos=256, sin=256, n=4, L=32: (  # noqa: E731
+        ctypes.byref(d), P(256), P(256), P(256), P(256), P(256), P(256), P(256), n, P(cos),
+        P(sin), L, None, None)
+    assert lib.pkv_append_rope(*args(cos=0)) == 1
+    assert lib.pkv_append_rope(*args(L=0)) == 1
+    assert lib.pkv_append_rope(*args(sin=264)) == 2
+    assert lib.pkv_append_rope(*args(n=-1)) == 1
+    assert lib.pkv_append_rope(*args(n=0)) == 0
