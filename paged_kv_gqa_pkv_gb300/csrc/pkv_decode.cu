@@ -23,17 +23,22 @@
 // kernel combines an item's segments by LSE.
 //
 // Arithmetic per tile: all G query heads of a kv head use one load of each K
-// and V row. The two products are small dense contractions
-// (S[G x 16] = Q[G x 128] K^T, O[G x 128] += P[G x 16] V) and run as warp-level
-// bf16 MMAs (m16n8k16, fp32 accumulate) with the G heads as the MMA rows;
-// K and V sit in shared memory in 128-byte-swizzled TMA boxes so ldmatrix
-// reads them without bank conflicts. The online softmax stays in fp32
-// registers: the row max is a quad shuffle reduction, exp2 with the scale
-// folded in, O rescaled only when some row's max moved. P goes from the S
-// accumulators straight into the A operand of the PV product (bf16), so the
-// softmax never touches shared memory. Keys past a row's length are masked to
-// -inf in S and their V rows are zeroed in shared memory before PV (stale
-// slots of a page may hold any bits, NaN included).
+// and V row. The two products are small dense contractions and run as
+// warp-level bf16 MMAs (m16n8k16, fp32 accumulate) in transposed form, so the
+// 16 tokens and the head dims fill the MMA's 16 rows and the G <= 8 heads its
+// 8 columns: S^T[16 x 8] = K Q^T over 8 k-steps, then O^T[128 x 8] += V^T P^T
+// as 8 m-tiles of one k-step (16 MMAs a tile; with the heads as rows it would
+// be 32, three quarters padding at G = 4). A warp first copies the tile's K
+// and V fragments out of shared memory (ldmatrix on 128-byte-swizzled TMA
+// boxes, conflict-free) and hands the stage back to TMA before any
+// arithmetic. The online softmax stays in fp32 registers: per-head max over
+// tokens is a 3-step shuffle reduction, exp2 with the scale folded in, O
+// rescaled only when some head's max moved. P^T leaves the S^T accumulators
+// as bf16 pairs and one register transpose (movmatrix) per 8 x 8 block makes
+// it the B operand of the PV product, so the softmax never touches shared
+// memory. Keys past a row's length are masked to -inf in S and their V rows
+// are zeroed in shared memory before the fragments are read (stale slots of a
+// page may hold any bits, NaN included).
 #include "pkv_launch.h"
 
 namespace pkv {
@@ -291,14 +296,16 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
     if (k + 1 < count) advance(pc, s_prefix, hkv);
   }
 
-  // MMA fragment coordinates: g = row (query head) of this lane's accumulators,
-  // t = its column pair.
+  // MMA fragment coordinates: g = this lane's accumulator row (a token in
+  // S^T, a head dim in O^T), t = its column pair (query heads 2t, 2t+1).
   const int g = lane >> 2;
   const int t = lane & 3;
-  const bool live_row = g < G;
-  uint32_t qa[8][2];     // A fragments of q (rows 0..G-1; rows >= G are zero)
-  float acc[16][4];      // O accumulators, n-tile = 8 head dims
-  float m_run = -INFINITY, l_run = 0.f;
+  const bool live_row = g < G;        // this lane loads q row g into the B fragments
+  const bool live_h0 = 2 * t < G;     // heads this lane's columns hold
+  const bool live_h1 = 2 * t + 1 < G;
+  uint32_t qb[8][2];     // B fragments of Q^T (columns 0..G-1; columns >= G are zero)
+  float acc[8][4];       // O^T accumulators, m-tile = 16 head dims
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
   int n_row = 0;
   int issued = prologue;
   // ldmatrix row addresses (per lane) within a K or V tile
@@ -320,106 +327,137 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
       const uint32_t* qs = reinterpret_cast<const uint32_t*>(st + C::kOffQ);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        qa[kk][0] = live_row ? qs[g * 64 + kk * 8 + t] : 0u;
-        qa[kk][1] = live_row ? qs[g * 64 + kk * 8 + 4 + t] : 0u;
+        qb[kk][0] = live_row ? qs[g * 64 + kk * 8 + t] : 0u;
+        qb[kk][1] = live_row ? qs[g * 64 + kk * 8 + 4 + t] : 0u;
       }
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt)
+      for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-      m_run = -INFINITY;
-      l_run = 0.f;
+        for (int e = 0; e < 4; ++e) acc[mt][e] = 0.f;
+      m_run[0] = m_run[1] = -INFINITY;
+      l_run[0] = l_run[1] = 0.f;
       n_row = s_len[cc.b];
     }
     const int n_valid = min(kDecodeTile, n_row - cc.tile * kDecodeTile);
-
-    // ---- S = Q K^T: two n-tiles of 8 tokens, 8 k-steps of 16 dims ----
-    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      uint32_t b0, b1, b2, b3;
-      // matrices: (tokens 0-7 | 8-15) x (dims 16kk..+7 | 16kk+8..+15)
-      ldsm_x4(sK + swz((mtx >> 1) * 8 + mrow, 2 * kk + (mtx & 1)), b0, b1, b2, b3);
-      mma_16816(sc[0], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
-      mma_16816(sc[1], qa[kk][0], 0u, qa[kk][1], 0u, b2, b3);
-    }
-    // ---- online softmax (log2 units) on rows g; columns t*2, t*2+1 (+8) ----
-    float x[4] = {sc[0][0] * p.qscale, sc[0][1] * p.qscale, sc[1][0] * p.qscale,
-                  sc[1][1] * p.qscale};
     if (n_valid < kDecodeTile) {
-      const int tok[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (tok[e] >= n_valid) x[e] = -INFINITY;
-      // stale slots past the row's end: zero their V rows before PV
+      // stale slots past the row's end may hold any bits (NaN included):
+      // zero their V rows before they are read (their scores are masked)
       for (int r = n_valid; r < kDecodeTile; ++r) {
         uint4* vrow = reinterpret_cast<uint4*>(st + C::kOffV);
         if (lane < 16) vrow[(swz(r, lane)) >> 4] = make_uint4(0u, 0u, 0u, 0u);
       }
       __syncwarp();
     }
-    float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float m_new = fmaxf(m_run, mx);
-    const float alpha = exp2f(m_run - m_new);  // 0 on the first tile
-    float pe[4];
+
+    // ---- the tile's K and V fragments into registers; the stage goes back
+    // to TMA before any arithmetic, so all S stages stay in flight ----
+    uint32_t kf[8][4], vf[8][4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) pe[e] = exp2f(x[e] - m_new);
-    l_run = l_run * alpha + ((pe[0] + pe[1]) + (pe[2] + pe[3]));
-    m_run = m_new;
-    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+    for (int kk = 0; kk < 8; ++kk)  // A = K: (tokens 0-7 | 8-15) x (dims 16kk..+7 | +8..+15)
+      ldsm_x4(sK + swz((mtx & 1) * 8 + mrow, 2 * kk + (mtx >> 1)), kf[kk][0], kf[kk][1],
+              kf[kk][2], kf[kk][3]);
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        acc[nt][0] *= alpha;
-        acc[nt][1] *= alpha;
+    for (int mt = 0; mt < 8; ++mt)  // A = V^T: (dims 16mt..+7 | +8..+15) x (tokens 0-7 | 8-15)
+      ldsm_x4_trans(sV + swz((mtx >> 1) * 8 + mrow, 2 * mt + (mtx & 1)), vf[mt][0], vf[mt][1],
+                    vf[mt][2], vf[mt][3]);
+    // these shared-memory reads (and the zeroing) come before the refill's
+    // async-proxy writes
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (k + S < count) {
+      issue(pc, k + S);
+      ++issued;
+      if (k + S + 1 < count) advance(pc, s_prefix, hkv);
+    }
+
+    // ---- S^T = K Q^T: 16 tokens x 8 head columns, 8 k-steps of 16 dims; even
+    // and odd k-steps accumulate separately to halve the dependent MMA chain ----
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    float sd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < 8; kk += 2) {
+      mma_16816(sc, kf[kk][0], kf[kk][1], kf[kk][2], kf[kk][3], qb[kk][0], qb[kk][1]);
+      mma_16816(sd, kf[kk + 1][0], kf[kk + 1][1], kf[kk + 1][2], kf[kk + 1][3], qb[kk + 1][0],
+                qb[kk + 1][1]);
+    }
+    // ---- online softmax (log2 units): x[0..1] token g, x[2..3] token g + 8;
+    // x[0], x[2] head 2t and x[1], x[3] head 2t + 1 ----
+    float x[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) x[e] = (sc[e] + sd[e]) * p.qscale;
+    if (g >= n_valid) x[0] = x[1] = -INFINITY;
+    if (g + 8 >= n_valid) x[2] = x[3] = -INFINITY;
+    float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+    const float alpha0 = exp2f(m_run[0] - mn0);  // 0 on the first tile
+    const float alpha1 = exp2f(m_run[1] - mn1);
+    const float pe0 = exp2f(x[0] - mn0), pe1 = exp2f(x[1] - mn1);
+    const float pe2 = exp2f(x[2] - mn0), pe3 = exp2f(x[3] - mn1);
+    l_run[0] = l_run[0] * alpha0 + (pe0 + pe2);
+    l_run[1] = l_run[1] * alpha1 + (pe1 + pe3);
+    m_run[0] = mn0;
+    m_run[1] = mn1;
+    if (__any_sync(0xffffffffu, alpha0 != 1.f || alpha1 != 1.f)) {
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        acc[mt][0] *= alpha0;
+        acc[mt][1] *= alpha1;
+        acc[mt][2] *= alpha0;
+        acc[mt][3] *= alpha1;
       }
     }
-    const uint32_t pa0 = pack_bf16x2(pe[0], pe[1]);  // P[g][2t..2t+1]
-    const uint32_t pa2 = pack_bf16x2(pe[2], pe[3]);  // P[g][8+2t..9+2t]
+    // P^T as the B operand: the S^T accumulator holds P^T[token][head]; a
+    // register transpose of each 8 x 8 block gives P[head][token] pairs
+    const uint32_t pb0 = movmatrix_trans(pack_bf16x2(pe0, pe1));  // tokens 0-7
+    const uint32_t pb1 = movmatrix_trans(pack_bf16x2(pe2, pe3));  // tokens 8-15
 
-    // ---- O += P V: 16 n-tiles of 8 dims, one k-step of 16 tokens ----
+    // ---- O^T += V^T P^T: 8 m-tiles of 16 dims, one k-step of 16 tokens ----
 #pragma unroll
-    for (int np = 0; np < 8; ++np) {
-      uint32_t b0, b1, b2, b3;
-      // matrices: (tokens 0-7 | 8-15) x (dims 16np..+7 | 16np+8..+15), transposed
-      ldsm_x4_trans(sV + swz((mtx & 1) * 8 + mrow, 2 * np + (mtx >> 1)), b0, b1, b2, b3);
-      mma_16816(acc[2 * np], pa0, 0u, pa2, 0u, b0, b1);
-      mma_16816(acc[2 * np + 1], pa0, 0u, pa2, 0u, b2, b3);
-    }
+    for (int mt = 0; mt < 8; ++mt)
+      mma_16816(acc[mt], vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3], pb0, pb1);
 
     // ---- segment end: leave the partial in slot worker + item ----
     const bool seg_end = (k == count - 1) || (cc.tile == cc.tiles - 1);
     if (seg_end) {
-      float lt = l_run;
-      lt += __shfl_xor_sync(0xffffffffu, lt, 1);
-      lt += __shfl_xor_sync(0xffffffffu, lt, 2);
+      float lt0 = l_run[0], lt1 = l_run[1];
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        lt0 += __shfl_xor_sync(0xffffffffu, lt0, o);
+        lt1 += __shfl_xor_sync(0xffffffffu, lt1, o);
+      }
       const int64_t slot_id = static_cast<int64_t>(worker) + static_cast<int64_t>(cc.b) * hkv + cc.kvh;
       float* slot = p.partials + slot_id * decode_slot_floats(G);
-      if (live_row) {
+      float* o0 = slot + (2 * t) * kHeadDim + g;
+      float* o1 = o0 + kHeadDim;
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt)
-          *reinterpret_cast<float2*>(slot + g * kHeadDim + nt * 8 + 2 * t) =
-              make_float2(acc[nt][0], acc[nt][1]);
-        if (t == 0) {
-          slot[G * kHeadDim + g] = m_run;
-          slot[G * kHeadDim + G + g] = lt;
+      for (int mt = 0; mt < 8; ++mt) {
+        if (live_h0) {
+          o0[16 * mt] = acc[mt][0];
+          o0[16 * mt + 8] = acc[mt][2];
+        }
+        if (live_h1) {
+          o1[16 * mt] = acc[mt][1];
+          o1[16 * mt + 8] = acc[mt][3];
+        }
+      }
+      if (g == 0) {
+        if (live_h0) {
+          slot[G * kHeadDim + 2 * t] = m_run[0];
+          slot[G * kHeadDim + G + 2 * t] = lt0;
+        }
+        if (live_h1) {
+          slot[G * kHeadDim + 2 * t + 1] = m_run[1];
+          slot[G * kHeadDim + G + 2 * t + 1] = lt1;
         }
       }
     }
     __syncwarp();
 
-    // ---- refill this stage with the tile S ahead ----
-    if (k + S < count) {
-      if (n_valid < kDecodeTile) {
-        // V rows zeroed above (generic proxy) must land before TMA refills them
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-      issue(pc, k + S);
-      ++issued;
-      if (k + S + 1 < count) advance(pc, s_prefix, hkv);
-    }
     if (k + 1 < count) advance(cc, s_prefix, hkv);
   }
 
