@@ -266,8 +266,6 @@ pkv_status pkv_decode_attention(const pkv_cache_desc* cache, const void* k_pool,
   st = encode_pool_map(&vmap, v_pool, cache);
   if (st != PKV_OK) return st;
 
-  const size_t slots = static_cast<size_t>(workers) + static_cast<size_t>(batch) * cache->num_kv_heads;
-  const size_t part_bytes = slots * pkv::decode_slot_floats(group) * sizeof(float);
   pkv::DecodeParams p;
   p.q = q;
   p.page_table = page_table;
@@ -276,7 +274,6 @@ pkv_status pkv_decode_attention(const pkv_cache_desc* cache, const void* k_pool,
   p.out = out;
   p.lse = lse;
   p.partials = static_cast<float*>(workspace);
-  p.prefix = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + ((part_bytes + 255) / 256) * 256);
   p.dev_err = dev_err;
   p.batch = batch;
   p.num_q_heads = num_q_heads;

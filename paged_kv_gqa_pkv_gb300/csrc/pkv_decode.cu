@@ -75,6 +75,19 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
                                (((chunk & 7) ^ (row & 7)) << 4));
 }
 
+// Tiles of row r and the device error its entries raise (0 if none). Both
+// kernels apply this one rule, so the merge can rebuild the split-KV pass's
+// schedule from the call's inputs alone.
+__device__ __forceinline__ int row_tiles(const DecodeParams& p, int r, int* err) {
+  const int c = p.batch_idx[r];
+  const int n = p.seq_lens[r];
+  *err = 0;
+  if (c < 0 || c >= p.max_batch) *err = PKV_DEV_ERR_BAD_SLOT;
+  else if (n < 0 || n > p.max_blocks * p.page_size) *err = PKV_DEV_ERR_BAD_POS;
+  else if (c != 0) return (n + kDecodeTile - 1) / kDecodeTile;
+  return 0;
+}
+
 // Position of a worker inside the tile list.
 struct Cursor {
   int b;      // row
@@ -196,18 +209,13 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
   const int per_thread = (B + blockDim.x - 1) / blockDim.x;
   const int r0 = min(tid * per_thread, B);
   const int r1 = min(r0 + per_thread, B);
-  const int max_len = p.max_blocks * p.page_size;
   int local = 0;
   for (int r = r0; r < r1; ++r) {
-    const int c = p.batch_idx[r];
-    const int n = p.seq_lens[r];
-    int tiles = 0, err = 0;
-    if (c < 0 || c >= p.max_batch) err = PKV_DEV_ERR_BAD_SLOT;
-    else if (n < 0 || n > max_len) err = PKV_DEV_ERR_BAD_POS;
-    else if (c != 0) tiles = (n + kDecodeTile - 1) / kDecodeTile;
+    int err;
+    const int tiles = row_tiles(p, r, &err);
     if (err && blockIdx.x == 0) set_dev_err(p.dev_err, err);
-    s_len[r] = n;
-    s_slot[r] = c;
+    s_len[r] = p.seq_lens[r];
+    s_slot[r] = p.batch_idx[r];
     s_prefix[r] = tiles;
     local += tiles;
   }
@@ -235,13 +243,7 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
   const int64_t per = (total + p.num_workers - 1) / p.num_workers;
   const int64_t u_begin = static_cast<int64_t>(worker) * per;
   const int64_t u_end = min(u_begin + per, total);
-  if (u_begin >= u_end) {
-    if (blockIdx.x == 0 && warp == 0) {
-      pdl_wait_primary();
-      for (int r = lane; r <= B; r += 32) p.prefix[r] = s_prefix[r];
-    }
-    return;
-  }
+  if (u_begin >= u_end) return;
   const int count = static_cast<int>(u_end - u_begin);
 
   const Cursor start = locate(s_prefix, B, hkv, u_begin);
@@ -287,9 +289,6 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
 
   load_row_pages(rp, p, s_slot, start.b, start.tiles, lane);
   pdl_wait_primary();
-  if (blockIdx.x == 0 && warp == 0) {
-    for (int r = lane; r <= B; r += 32) p.prefix[r] = s_prefix[r];
-  }
   const int prologue = min(S, count);
   for (int k = 0; k < prologue; ++k) {
     issue(pc, k);
@@ -307,6 +306,7 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
   float acc[8][4];       // O^T accumulators, m-tile = 16 head dims
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
   int n_row = 0;
+  int seg_t0 = 0;  // first tile of the open segment
   int issued = prologue;
   // ldmatrix row addresses (per lane) within a K or V tile
   const int mtx = lane >> 3;       // which of the four 8x8 matrices this lane addresses
@@ -337,6 +337,7 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
       m_run[0] = m_run[1] = -INFINITY;
       l_run[0] = l_run[1] = 0.f;
       n_row = s_len[cc.b];
+      seg_t0 = cc.tile;
     }
     const int n_valid = min(kDecodeTile, n_row - cc.tile * kDecodeTile);
     if (n_valid < kDecodeTile) {
@@ -430,29 +431,55 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
         lt0 += __shfl_xor_sync(0xffffffffu, lt0, o);
         lt1 += __shfl_xor_sync(0xffffffffu, lt1, o);
       }
-      const int64_t slot_id = static_cast<int64_t>(worker) + static_cast<int64_t>(cc.b) * hkv + cc.kvh;
-      float* slot = p.partials + slot_id * decode_slot_floats(G);
-      float* o0 = slot + (2 * t) * kHeadDim + g;
-      float* o1 = o0 + kHeadDim;
+      if (seg_t0 == 0 && cc.tile == cc.tiles - 1) {
+        // the item lies in this segment alone: normalise and write it out
+        // here (the merge skips items of one segment)
+        const float inv0 = 1.f / lt0, inv1 = 1.f / lt1;
+        const int64_t head0 = static_cast<int64_t>(cc.b) * p.num_q_heads + cc.kvh * G + 2 * t;
+        __nv_bfloat16* o0 = static_cast<__nv_bfloat16*>(p.out) + head0 * kHeadDim + g;
+        __nv_bfloat16* o1 = o0 + kHeadDim;
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        if (live_h0) {
-          o0[16 * mt] = acc[mt][0];
-          o0[16 * mt + 8] = acc[mt][2];
+        for (int mt = 0; mt < 8; ++mt) {
+          if (live_h0) {
+            o0[16 * mt] = __float2bfloat16_rn(acc[mt][0] * inv0);
+            o0[16 * mt + 8] = __float2bfloat16_rn(acc[mt][2] * inv0);
+          }
+          if (live_h1) {
+            o1[16 * mt] = __float2bfloat16_rn(acc[mt][1] * inv1);
+            o1[16 * mt + 8] = __float2bfloat16_rn(acc[mt][3] * inv1);
+          }
         }
-        if (live_h1) {
-          o1[16 * mt] = acc[mt][1];
-          o1[16 * mt + 8] = acc[mt][3];
+        if (g == 0) {
+          if (live_h0) p.lse[head0] = (m_run[0] + log2f(lt0)) * 0.69314718055994531f;
+          if (live_h1) p.lse[head0 + 1] = (m_run[1] + log2f(lt1)) * 0.69314718055994531f;
         }
-      }
-      if (g == 0) {
-        if (live_h0) {
-          slot[G * kHeadDim + 2 * t] = m_run[0];
-          slot[G * kHeadDim + G + 2 * t] = lt0;
+      } else {
+        // leave the partial in slot worker + item
+        const int64_t slot_id =
+            static_cast<int64_t>(worker) + static_cast<int64_t>(cc.b) * hkv + cc.kvh;
+        float* slot = p.partials + slot_id * decode_slot_floats(G);
+        float* o0 = slot + (2 * t) * kHeadDim + g;
+        float* o1 = o0 + kHeadDim;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          if (live_h0) {
+            o0[16 * mt] = acc[mt][0];
+            o0[16 * mt + 8] = acc[mt][2];
+          }
+          if (live_h1) {
+            o1[16 * mt] = acc[mt][1];
+            o1[16 * mt + 8] = acc[mt][3];
+          }
         }
-        if (live_h1) {
-          slot[G * kHeadDim + 2 * t + 1] = m_run[1];
-          slot[G * kHeadDim + G + 2 * t + 1] = lt1;
+        if (g == 0) {
+          if (live_h0) {
+            slot[G * kHeadDim + 2 * t] = m_run[0];
+            slot[G * kHeadDim + G + 2 * t] = lt0;
+          }
+          if (live_h1) {
+            slot[G * kHeadDim + 2 * t + 1] = m_run[1];
+            slot[G * kHeadDim + G + 2 * t + 1] = lt1;
+          }
         }
       }
     }
@@ -470,26 +497,40 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
   }
 }
 
-// One warp per (row, q head): lanes load the segments' (m, l) in parallel,
-// the o loads of the first segments go out in the same round, and the LSE
-// combination is a warp reduction.
+// One warp per (row, q head). The warp rebuilds the split-KV schedule from
+// the call's inputs (row tile counts and their prefix) before waiting on the
+// split-KV grid, so after the wait only the partials are read: for items of
+// up to 8 segments, (m, l) and all o rows go out in one round of loads.
 template <int G>
 __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p) {
   // The next launch may start its prologue now; it touches the workspace
   // only after this grid completes.
   pdl_launch_dependents();
-  pdl_wait_primary();
   const int lane = threadIdx.x & 31;
   const int wid = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (wid >= p.batch * p.num_q_heads) return;
-  const int b = wid / p.num_q_heads;
+  const int B = p.batch;
+  const bool active = wid < B * p.num_q_heads;
+  const int b = active ? wid / p.num_q_heads : 0;
   const int h = wid % p.num_q_heads;
   const int kvh = h / G;
   const int g = h % G;
   const int hkv = p.num_kv_heads;
-  const int pb = p.prefix[b];
-  const int tiles = p.prefix[b + 1] - pb;
-  const int64_t total = static_cast<int64_t>(p.prefix[p.batch]) * hkv;
+  int before = 0, total = 0, tiles = 0;
+  for (int r = lane; r < B; r += 32) {
+    int err;
+    const int t = row_tiles(p, r, &err);
+    total += t;
+    if (r < b) before += t;
+    if (r == b) tiles = t;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    total += __shfl_xor_sync(0xffffffffu, total, o);
+    before += __shfl_xor_sync(0xffffffffu, before, o);
+    tiles += __shfl_xor_sync(0xffffffffu, tiles, o);
+  }
+  pdl_wait_primary();
+  if (!active) return;
   __nv_bfloat16* out =
       static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(wid) * kHeadDim + lane * 4;
   if (tiles == 0) {
@@ -497,41 +538,71 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
     if (lane == 0) p.lse[wid] = -INFINITY;
     return;
   }
-  const int64_t per = (total + p.num_workers - 1) / p.num_workers;
-  const int64_t u0 = static_cast<int64_t>(pb) * hkv + static_cast<int64_t>(kvh) * tiles;
+  const int64_t per = (static_cast<int64_t>(total) * hkv + p.num_workers - 1) / p.num_workers;
+  const int64_t u0 = static_cast<int64_t>(before) * hkv + static_cast<int64_t>(kvh) * tiles;
   const int w0 = static_cast<int>(u0 / per);
   const int nseg = static_cast<int>((u0 + tiles - 1) / per) - w0 + 1;
+  if (nseg == 1) return;  // written by the split-KV pass
   constexpr int SF = decode_slot_floats(G);
   const float* slots = p.partials + (static_cast<int64_t>(w0) + static_cast<int64_t>(b) * hkv + kvh) * SF;
 
-  float M = -INFINITY;
-  for (int s0 = 0; s0 < nseg; s0 += 32) {
-    const int s = s0 + lane;
-    if (s < nseg) M = fmaxf(M, slots[static_cast<int64_t>(s) * SF + G * kHeadDim + g]);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-
-  float L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = 0; s0 < nseg; s0 += 32) {
-    const int s = s0 + lane;
-    float sc = 0.f;
-    if (s < nseg) {
-      const float* sl = slots + static_cast<int64_t>(s) * SF;
-      sc = exp2f(sl[G * kHeadDim + g] - M);
-      L = fmaf(sl[G * kHeadDim + G + g], sc, L);
+  float M, L = 0.f;
+  if (nseg <= 8) {
+    float ms = -INFINITY, ls = 0.f;
+    if (lane < nseg) {
+      ms = __ldcg(slots + static_cast<int64_t>(lane) * SF + G * kHeadDim + g);
+      ls = __ldcg(slots + static_cast<int64_t>(lane) * SF + G * kHeadDim + G + g);
     }
-    const int n = min(32, nseg - s0);
-#pragma unroll 4
-    for (int j = 0; j < n; ++j) {
+    float4 ov[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < nseg)
+        ov[j] = __ldcg(reinterpret_cast<const float4*>(slots + static_cast<int64_t>(j) * SF +
+                                                       g * kHeadDim + lane * 4));
+    M = ms;
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    M = __shfl_sync(0xffffffffu, M, 0);
+    const float sc = (lane < nseg) ? exp2f(ms - M) : 0.f;
+    L = ls * sc;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
       const float scj = __shfl_sync(0xffffffffu, sc, j);
-      const float4 ov = *reinterpret_cast<const float4*>(
-          slots + static_cast<int64_t>(s0 + j) * SF + g * kHeadDim + lane * 4);
-      acc.x = fmaf(ov.x, scj, acc.x);
-      acc.y = fmaf(ov.y, scj, acc.y);
-      acc.z = fmaf(ov.z, scj, acc.z);
-      acc.w = fmaf(ov.w, scj, acc.w);
+      if (j < nseg) {
+        acc.x = fmaf(ov[j].x, scj, acc.x);
+        acc.y = fmaf(ov[j].y, scj, acc.y);
+        acc.z = fmaf(ov[j].z, scj, acc.z);
+        acc.w = fmaf(ov[j].w, scj, acc.w);
+      }
+    }
+  } else {
+    M = -INFINITY;
+    for (int s0 = 0; s0 < nseg; s0 += 32) {
+      const int s = s0 + lane;
+      if (s < nseg) M = fmaxf(M, __ldcg(slots + static_cast<int64_t>(s) * SF + G * kHeadDim + g));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    for (int s0 = 0; s0 < nseg; s0 += 32) {
+      const int s = s0 + lane;
+      float sc = 0.f;
+      if (s < nseg) {
+        const float* sl = slots + static_cast<int64_t>(s) * SF;
+        sc = exp2f(__ldcg(sl + G * kHeadDim + g) - M);
+        L = fmaf(__ldcg(sl + G * kHeadDim + G + g), sc, L);
+      }
+      const int n = min(32, nseg - s0);
+#pragma unroll 4
+      for (int j = 0; j < n; ++j) {
+        const float scj = __shfl_sync(0xffffffffu, sc, j);
+        const float4 ov = __ldcg(reinterpret_cast<const float4*>(
+            slots + static_cast<int64_t>(s0 + j) * SF + g * kHeadDim + lane * 4));
+        acc.x = fmaf(ov.x, scj, acc.x);
+        acc.y = fmaf(ov.y, scj, acc.y);
+        acc.z = fmaf(ov.z, scj, acc.z);
+        acc.w = fmaf(ov.w, scj, acc.w);
+      }
     }
   }
 #pragma unroll
@@ -549,8 +620,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
 size_t decode_workspace_bytes(int batch, int num_kv_heads, int group, int num_workers) {
   const size_t slots = static_cast<size_t>(num_workers) + static_cast<size_t>(batch) * num_kv_heads;
   const size_t part = slots * decode_slot_floats(group) * sizeof(float);
-  const size_t pre = (static_cast<size_t>(batch) + 1) * sizeof(int32_t);
-  return ((part + 255) / 256) * 256 + ((pre + 255) / 256) * 256;
+  return ((part + 255) / 256) * 256;
 }
 
 int decode_workers_for_device(int sm_count) { return sm_count * kDecodeWarps; }

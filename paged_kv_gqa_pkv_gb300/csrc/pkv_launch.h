@@ -52,7 +52,6 @@ struct DecodeParams {
   void* out;                  // bf16 [B, Hq, D]
   float* lse;                 // [B, Hq]
   float* partials;            // workspace: (num_workers + B*Hkv) slots
-  int32_t* prefix;            // workspace: [B + 1] tile prefix over rows
   int32_t* dev_err;
   int batch;
   int num_q_heads;

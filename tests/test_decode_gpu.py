@@ -156,3 +156,47 @@ def test_decode_rejects_bad_host_arguments():
     with pytest.raises(binding.PkvError) as e:   # group 3 unsupported
         binding.pkv_decode_attention(kp, vp, table, q6, bidx, lens, c.page_size, c.scale)
     assert e.value.status == 1
+
+
+def _decode_with(case, ws, err):
+    kp, vp, table = gpu(case.k_pool), gpu(case.v_pool), gpu(case.page_table)
+    return binding.pkv_decode_attention(kp, vp, table, gpu(case.q), gpu(case.batch_idx),
+                                        gpu(case.seq_lens), case.page_size, case.scale,
+                                        workspace=ws, dev_err=err)
+
+
+def test_one_workspace_serves_every_shape():
+    """One workspace (uninitialised) across batch sizes, GQA groups and KV-head
+    counts: nothing of a call's scratch may leak into the next."""
+    shapes = [(64, 32, 8, 600), (3, 32, 8, 9000), (200, 8, 8, 300), (1, 16, 2, 5000),
+              (17, 64, 8, 1200), (64, 32, 8, 600)]
+    cases = []
+    for i, (B, hq, hkv, lmax) in enumerate(shapes):
+        lens = torch.randint(1, lmax, (B,), generator=torch.Generator().manual_seed(i)).tolist()
+        cases.append(W.custom_decode(40 + i, lens, hq=hq, hkv=hkv, page_size=128, permute=True))
+    need = max(binding.pkv_decode_workspace_size(gpu(c.k_pool), gpu(c.page_table), 128,
+                                                 c.batch, c.num_q_heads) for c in cases)
+    ws = torch.full((need,), 0x7f, dtype=torch.uint8, device="cuda")
+    for c in cases:
+        err = new_dev_err()
+        out, lse = _decode_with(c, ws, err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        _, _, ref_o, ref_l, _, _ = oracle_decode_step(c, append=False)
+        assert_attention_close(out.cpu(), lse.cpu(), ref_o, ref_l, tag=c.name)
+
+
+def test_single_long_row_merges_many_segments():
+    """One 8192-key row: each item is cut into ~128 segments, more than one
+    merge pass of 32 lanes."""
+    c = W.custom_decode(21, [8192], hq=32, hkv=8, page_size=128, permute=True)
+    _full_parity(c)
+
+
+def test_short_rows_finish_whole_items_in_one_worker():
+    """512 rows of 1..40 keys: most items fall inside one worker's range and
+    are normalised without a partial."""
+    lens = torch.randint(1, 41, (512,), generator=torch.Generator().manual_seed(5)).tolist()
+    c = W.custom_decode(23, lens, hq=32, hkv=8, page_size=16, permute=True)
+    _full_parity(c)
+
