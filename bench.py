@@ -1,8 +1,11 @@
 """Benchmark: one decode step of a paged-KV GQA attention layer, Qwen3-4B shape.
 
-A step is the whole hot path on one batch: ``pkv_append`` of the 64 new
-tokens' K/V through the page table, then ``pkv_decode_attention`` (split-KV
-pass over the pages + LSE merge). Workload: B=64, Hq=32, Hkv=8, D=128,
+A step is the whole hot path on one batch, as one call:
+``pkv_decode_append_attention`` writes the 64 new tokens' K/V through the page
+table and runs the split-KV decode over the pages including them, then the
+LSE merge (two kernels). The two-call step (``pkv_append``, then
+``pkv_decode_attention``) and the decode call alone are timed beside it.
+Workload: B=64, Hq=32, Hkv=8, D=128,
 page 128, keys attended uniform in [512, 1024], sequential pages (a fresh
 batch's allocation, the contiguous fast path); a second line of numbers is
 taken with randomly permuted pages, and the packed document-causal prefill
@@ -34,7 +37,8 @@ sys.path.insert(0, ROOT)
 METRIC = "decode-attn KV GB/s & % of HBM peak; tokens/s/layer at B=64 Qwen3-4B shape"
 UNIT = "GB/s"
 WORKLOAD = ("qwen3_b64_decode: B=64, Hq=32, Hkv=8, D=128, page_size=128, keys U[512,1024], "
-            "sequential pages, seed 0; step = append 64 tokens + split-KV decode")
+            "sequential pages, seed 0; step = one fused call: append 64 tokens + split-KV "
+            "decode + merge")
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -255,9 +259,10 @@ def run_pkv(args):
         return 2 * case.k_pool.numel() * 2
 
     def timed_decode(case, steps, warmup):
-        """Times `steps` decode steps (append + decode) replayed from CUDA
-        graphs, rotating over pool sets so each step's KV comes from HBM; a
-        second graph of decode calls alone gives the decode call's duration."""
+        """Times `steps` decode steps (the fused append + decode call) replayed
+        from CUDA graphs, rotating over pool sets so each step's KV comes from
+        HBM; a second graph of decode calls alone gives the decode call's
+        duration, and a third the two-call step (append, then decode)."""
         n_sets = max(2, math.ceil(2 * L2_BYTES / kv_set_bytes(case)) + 1)
         sets = make_sets(case, n_sets)
         B, hq = case.batch, case.num_q_heads
@@ -279,9 +284,17 @@ def run_pkv(args):
                                          case.page_size, case.scale, out=out, lse=lse,
                                          workspace=ws, dev_err=err)
 
+        def fused(i):
+            s = sets[i % n_sets]
+            binding.pkv_decode_append_attention(s["kp"], s["vp"], s["pt"], s["q"], s["kn"],
+                                                s["vn"], s["bi"], s["sl"], case.page_size,
+                                                case.scale, out=out, lse=lse, workspace=ws,
+                                                dev_err=err)
+
         for i in range(max(warmup, n_sets)):   # eager warm-up (first-call set-up)
             append(i)
             decode(i)
+            fused(i)
         torch.cuda.synchronize()
 
         per_graph = n_sets * max(1, 96 // n_sets)
@@ -293,13 +306,15 @@ def run_pkv(args):
                     body(i)
             return g
 
-        step_g = capture(per_graph, lambda i: (append(i), decode(i)))
+        step_g = capture(per_graph, fused)
         tail = steps % per_graph
-        tail_g = capture(tail, lambda i: (append(i), decode(i))) if tail else None
+        tail_g = capture(tail, fused) if tail else None
         dec_g = capture(per_graph, decode)
+        two_g = capture(per_graph, lambda i: (append(i), decode(i)))
         for _ in range(max(1, warmup // per_graph)):
             step_g.replay()
             dec_g.replay()
+            two_g.replay()
         torch.cuda.synchronize()
 
         t0 = torch.cuda.Event(enable_timing=True)
@@ -317,21 +332,24 @@ def run_pkv(args):
             torch.cuda.synchronize()
         total_ms = t0.elapsed_time(t1)
 
-        # decode calls alone, same graph shape; several timed replays
+        # decode calls alone and the two-call step, same graph shape; several
+        # timed replays each
         reps = max(3, min(50, steps // per_graph))
-        dec_ms = []
+        dec_ms, two_ms = [], []
         for _ in range(reps):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record()
-            dec_g.replay()
-            b.record()
-            torch.cuda.synchronize()
-            dec_ms.append(a.elapsed_time(b) / per_graph)
+            for g, acc in ((dec_g, dec_ms), (two_g, two_ms)):
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record()
+                g.replay()
+                b.record()
+                torch.cuda.synchronize()
+                acc.append(a.elapsed_time(b) / per_graph)
         if int(err.item()) != 0:
             raise RuntimeError(f"device error bits {int(err.item()):#x} during the bench")
         dec_sorted = sorted(dec_ms)
         return dict(total_ms=total_ms, dec_ms=statistics.median(dec_ms),
+                    two_call_ms=statistics.median(two_ms),
                     dec_p10=dec_sorted[len(dec_ms) // 10],
                     dec_p90=dec_sorted[(9 * len(dec_ms)) // 10],
                     clocks=clk.summary(), n_sets=n_sets, set_bytes=kv_set_bytes(case),
@@ -343,7 +361,7 @@ def run_pkv(args):
         s = make_sets(case, 1)[0]
         host = {k: getattr(case, a).pin_memory() for k, a in
                 (("q", "q"), ("kn", "k_new"), ("vn", "v_new"), ("bi", "batch_idx"),
-                 ("ip", "input_pos"), ("sl", "seq_lens"), ("pt", "page_table"))}
+                 ("sl", "seq_lens"), ("pt", "page_table"))}
         B, hq = case.batch, case.num_q_heads
         out_h = torch.empty((B, hq, 128), dtype=torch.bfloat16).pin_memory()
         lse_h = torch.empty((B, hq), dtype=torch.float32).pin_memory()
@@ -358,11 +376,10 @@ def run_pkv(args):
         def step():
             for k, t in host.items():
                 s[k].copy_(t, non_blocking=True)
-            binding.pkv_append(s["kp"], s["vp"], s["pt"], s["kn"], s["vn"], s["bi"], s["ip"],
-                               case.page_size, stream=stream)
-            binding.pkv_decode_attention(s["kp"], s["vp"], s["pt"], s["q"], s["bi"], s["sl"],
-                                         case.page_size, case.scale, out=out, lse=lse,
-                                         workspace=ws, stream=stream)
+            binding.pkv_decode_append_attention(s["kp"], s["vp"], s["pt"], s["q"], s["kn"],
+                                                s["vn"], s["bi"], s["sl"], case.page_size,
+                                                case.scale, out=out, lse=lse, workspace=ws,
+                                                stream=stream)
             out_h.copy_(out, non_blocking=True)
             lse_h.copy_(lse, non_blocking=True)
             stream.synchronize()
@@ -452,7 +469,7 @@ def run_pkv(args):
         "tokens_per_s_per_layer": world * case.batch / (ms_step * 1e-3),
         "decode_call_us": r["dec_ms"] * 1e3, "decode_call_us_p10_p90": [r["dec_p10"] * 1e3,
                                                                          r["dec_p90"] * 1e3],
-        "append_call_us_est": (ms_step - r["dec_ms"]) * 1e3,
+        "two_call_step_us": r["two_call_ms"] * 1e3,
         "timing": f"CUDA-graph replay of {r['per_graph']}-step graphs; decode call = replay "
                   f"of {r['per_graph']} decode calls / {r['per_graph']}",
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
@@ -467,7 +484,7 @@ def run_pkv(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
         "prefill": prefill,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,
         "clocks": r["clocks"],
     }
     if not args.no_cpu_baseline:

@@ -169,6 +169,34 @@ pkv_status pkv_decode_attention(const pkv_cache_desc* cache, const void* k_pool,
                                 cudaStream_t stream);
 
 /*
+ * pkv_decode_append_attention - one decode step's KV append fused into the
+ * decode attention (one launch fewer than pkv_append + pkv_decode_attention).
+ * Source: the pages' decode step writes the new token's K/V into the paged
+ * cache, then attends over the cache including it ("qwen3_flex_inference.py",
+ * forward "Write to paged KV cache" then flex_attention with
+ * _decode_block_mask); fusing the two is the survey's next step after graphs.
+ *
+ * Same arguments and results as pkv_decode_attention, plus k_new, v_new:
+ * bf16 [batch, num_kv_heads, D], 16-byte aligned. Row b's new token is
+ * written to position seq_lens[b] - 1 of slot batch_idx[b] (a decode step has
+ * seq_lens[b] = input_pos[b] + 1), exactly as pkv_append would write it
+ * (bit-exact byte copy), and the attention of row b includes it. Rows that
+ * attend nothing (batch_idx 0, seq_lens 0, or rejected entries) write
+ * nothing. A page entry for the new position outside [0, num_pages) skips
+ * that write and sets PKV_DEV_ERR_BAD_PAGE. The pools are written, so they
+ * are non-const here; k_pool/v_pool must not alias k_new/v_new.
+ */
+pkv_status pkv_decode_append_attention(const pkv_cache_desc* cache, void* k_pool,
+                                       void* v_pool, const int32_t* page_table,
+                                       const void* q, int num_q_heads,
+                                       const void* k_new, const void* v_new,
+                                       const int32_t* batch_idx,
+                                       const int32_t* seq_lens, int batch,
+                                       float scale, void* out, float* lse,
+                                       void* workspace, size_t workspace_bytes,
+                                       int32_t* dev_err, cudaStream_t stream);
+
+/*
  * pkv_decode_attention_static_scratch - pkv_decode_attention for callers that
  * cannot allocate device memory. The source pages have no counterpart: this
  * is a deployment convenience of this library.

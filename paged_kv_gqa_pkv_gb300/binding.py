@@ -6,7 +6,8 @@ runs in the library's CUDA kernels on the caller's current stream. There is
 no fallback: if ``libpkv.so`` is missing or fails to load, every call raises.
 
 Functions keep the names of the C entry points:
-``pkv_append``, ``pkv_decode_attention``, ``pkv_decode_workspace_size``,
+``pkv_append``, ``pkv_decode_attention``, ``pkv_decode_append_attention``,
+``pkv_decode_workspace_size``,
 ``pkv_prefill_attention``, ``pkv_status_string``.
 """
 
@@ -31,6 +32,7 @@ DEV_ERR_LAYOUT = 0x8
 DEV_ERR_TIMEOUT = 0x10
 
 EXPORTED = ("pkv_append", "pkv_append_rope", "pkv_decode_workspace_size", "pkv_decode_attention",
+            "pkv_decode_append_attention",
             "pkv_prefill_attention", "pkv_status_string",
             "pkv_status_from_device_error", "pkv_last_cuda_error_string")
 
@@ -77,6 +79,10 @@ def load_library() -> ctypes.CDLL:
     lib.pkv_decode_attention.argtypes = [desc_p, vp, vp, i32p, vp, c_int, i32p, i32p, c_int,
                                          c_float, vp, f32p, vp, c_size, i32p, vp]
     lib.pkv_decode_attention.restype = c_int
+    lib.pkv_decode_append_attention.argtypes = [desc_p, vp, vp, i32p, vp, c_int, vp, vp, i32p,
+                                                i32p, c_int, c_float, vp, f32p, vp, c_size, i32p,
+                                                vp]
+    lib.pkv_decode_append_attention.restype = c_int
     lib.pkv_prefill_attention.argtypes = [vp, vp, vp, c_int, c_int, c_int, i32p, i32p, c_int,
                                           c_float, vp, f32p, i32p, vp]
     lib.pkv_prefill_attention.restype = c_int
@@ -213,6 +219,42 @@ def pkv_decode_attention(k_pool, v_pool, page_table, q, batch_idx, seq_lens,
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_err),
         _stream(stream))
     _check("pkv_decode_attention", st)
+    return out, lse
+
+
+def pkv_decode_append_attention(k_pool, v_pool, page_table, q, k_new, v_new, batch_idx,
+                                seq_lens, page_size: int, scale: float, out=None, lse=None,
+                                workspace=None, dev_err=None, stream=None):
+    """One decode step in one call: row b's new token (k_new/v_new
+    [B, Hkv, D] bf16) is written to position seq_lens[b] - 1 of its slot and
+    attended with the rest. Returns (out [B, Hq, D] bf16, lse [B, Hq] fp32)."""
+    _need(q, "q", torch.bfloat16, 3)
+    for name, t, dt, nd in (("k_pool", k_pool, torch.bfloat16, 3),
+                            ("v_pool", v_pool, torch.bfloat16, 3),
+                            ("k_new", k_new, torch.bfloat16, 3),
+                            ("v_new", v_new, torch.bfloat16, 3),
+                            ("page_table", page_table, torch.int32, 2),
+                            ("batch_idx", batch_idx, torch.int32, 1),
+                            ("seq_lens", seq_lens, torch.int32, 1)):
+        _need(t, name, dt, nd)
+    B, hq, d = q.shape
+    if k_new.shape != (B, k_pool.shape[1], d) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [B, Hkv, D]")
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, hq), dtype=torch.float32, device=q.device)
+    desc = cache_desc(k_pool, page_table, page_size)
+    lib = load_library()
+    if workspace is None:
+        n = lib.pkv_decode_workspace_size(ctypes.byref(desc), B, hq, 0)
+        workspace = torch.empty(max(int(n), 256), dtype=torch.uint8, device=q.device)
+    st = lib.pkv_decode_append_attention(
+        ctypes.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(q), hq,
+        _ptr(k_new), _ptr(v_new), _ptr(batch_idx), _ptr(seq_lens), B, float(scale), _ptr(out),
+        _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_err),
+        _stream(stream))
+    _check("pkv_decode_append_attention", st)
     return out, lse
 
 

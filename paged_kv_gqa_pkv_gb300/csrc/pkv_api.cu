@@ -88,21 +88,21 @@ bool group_ok(int num_q_heads, int num_kv_heads) {
   return g == 1 || g == 2 || g == 4 || g == 8;
 }
 
-// 3-D view {D, H_kv, rows} of a token-major pool; a box is 16 rows of one head
-// and half its head dims, 128-byte swizzled (the layout ldmatrix reads).
 pkv_status encode_pool_map(CUtensorMap* map, const void* pool, const pkv_cache_desc* c) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (enc == nullptr) return PKV_ERR_CUDA;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(c->head_dim),
-                              static_cast<cuuint64_t>(c->num_kv_heads),
-                              static_cast<cuuint64_t>(c->num_pages) * c->page_size};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(c->head_dim) * 2,
-                                 static_cast<cuuint64_t>(c->num_kv_heads) * c->head_dim * 2};
-  // 64 head dims x 1 head x 16 tokens: one 128-byte-swizzled half of a tile
-  const cuuint32_t box[3] = {64u, 1u, static_cast<cuuint32_t>(pkv::kDecodeTile)};
-  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  // 4-D view {64 dims, rows, 2 halves of the head dims, H_kv}: the halves get
+  // their own axis (stride 128 B) so that one box {64, 16 tokens, 2, 1} is a
+  // whole 16-token tile of one head, landing as two 128-byte-swizzled
+  // [16 rows x 128 B] halves, the layout ldmatrix reads.
+  const cuuint64_t dims[4] = {64u, static_cast<cuuint64_t>(c->num_pages) * c->page_size, 2u,
+                              static_cast<cuuint64_t>(c->num_kv_heads)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(c->num_kv_heads) * c->head_dim * 2,
+                                 128u, static_cast<cuuint64_t>(c->head_dim) * 2};
+  const cuuint32_t box[4] = {64u, static_cast<cuuint32_t>(pkv::kDecodeTile), 2u, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   std::memset(map, 0, sizeof(*map));
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims,
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(pool), dims,
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -118,6 +118,70 @@ pkv_status record_cuda_status(cudaError_t e) {
   return PKV_ERR_CUDA;
 }
 }  // namespace pkv
+
+namespace {
+
+// Shared by the attention-only and the append-fused entry points: k_new and
+// v_new null means attention alone (the pools are then only read).
+pkv_status decode_entry(const pkv_cache_desc* cache, const void* k_pool, const void* v_pool,
+                        const int32_t* page_table, const void* q, int num_q_heads,
+                        const void* k_new, const void* v_new, const int32_t* batch_idx,
+                        const int32_t* seq_lens, int batch, float scale, void* out, float* lse,
+                        void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                        cudaStream_t stream) {
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (batch < 0 || batch > pkv::kDecodeMaxBatch) return PKV_ERR_ARG;
+  if (!group_ok(num_q_heads, cache->num_kv_heads)) return PKV_ERR_ARG;
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return PKV_ERR_ARG;
+  if (batch == 0) return PKV_OK;
+  if (!k_pool || !v_pool || !page_table || !q || !batch_idx || !seq_lens || !out || !lse)
+    return PKV_ERR_ARG;
+  if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(q, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4) || !aligned(page_table, 4) || !aligned(batch_idx, 4) ||
+      !aligned(seq_lens, 4) || !aligned(dev_err, 4))
+    return PKV_ERR_ALIGN;
+  int sms = 0;
+  st = device_info(&sms);
+  if (st != PKV_OK) return st;
+  const int group = num_q_heads / cache->num_kv_heads;
+  const int workers = pkv::decode_workers_for_device(sms);
+  const size_t need = pkv::decode_workspace_bytes(batch, cache->num_kv_heads, group, workers);
+  if (workspace == nullptr || workspace_bytes < need) return PKV_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return PKV_ERR_ALIGN;
+
+  CUtensorMap kmap, vmap;
+  st = encode_pool_map(&kmap, k_pool, cache);
+  if (st != PKV_OK) return st;
+  st = encode_pool_map(&vmap, v_pool, cache);
+  if (st != PKV_OK) return st;
+
+  pkv::DecodeParams p;
+  p.q = q;
+  p.page_table = page_table;
+  p.batch_idx = batch_idx;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.lse = lse;
+  p.partials = static_cast<float*>(workspace);
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.k_pool = const_cast<void*>(k_pool);
+  p.v_pool = const_cast<void*>(v_pool);
+  p.dev_err = dev_err;
+  p.batch = batch;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = cache->num_kv_heads;
+  p.page_size = cache->page_size;
+  p.num_pages = cache->num_pages;
+  p.max_batch = cache->max_batch;
+  p.max_blocks = cache->max_blocks;
+  p.num_workers = workers;
+  p.qscale = scale * 1.4426950408889634f;
+  return cuda_status(pkv::launch_decode(p, kmap, vmap, sms, stream));
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -233,58 +297,30 @@ size_t pkv_decode_workspace_size(const pkv_cache_desc* cache, int batch, int num
                                      pkv::decode_workers_for_device(sms));
 }
 
+
 pkv_status pkv_decode_attention(const pkv_cache_desc* cache, const void* k_pool,
                                 const void* v_pool, const int32_t* page_table, const void* q,
                                 int num_q_heads, const int32_t* batch_idx,
                                 const int32_t* seq_lens, int batch, float scale, void* out,
                                 float* lse, void* workspace, size_t workspace_bytes,
                                 int32_t* dev_err, cudaStream_t stream) {
-  pkv_status st = check_cache(cache);
-  if (st != PKV_OK) return st;
-  if (batch < 0 || batch > pkv::kDecodeMaxBatch) return PKV_ERR_ARG;
-  if (!group_ok(num_q_heads, cache->num_kv_heads)) return PKV_ERR_ARG;
-  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return PKV_ERR_ARG;
-  if (batch == 0) return PKV_OK;
-  if (!k_pool || !v_pool || !page_table || !q || !batch_idx || !seq_lens || !out || !lse)
-    return PKV_ERR_ARG;
-  if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(q, 16) || !aligned(out, 16) ||
-      !aligned(lse, 4) || !aligned(page_table, 4) || !aligned(batch_idx, 4) ||
-      !aligned(seq_lens, 4) || !aligned(dev_err, 4))
-    return PKV_ERR_ALIGN;
-  int sms = 0;
-  st = device_info(&sms);
-  if (st != PKV_OK) return st;
-  const int group = num_q_heads / cache->num_kv_heads;
-  const int workers = pkv::decode_workers_for_device(sms);
-  const size_t need = pkv::decode_workspace_bytes(batch, cache->num_kv_heads, group, workers);
-  if (workspace == nullptr || workspace_bytes < need) return PKV_ERR_WORKSPACE;
-  if (!aligned(workspace, 256)) return PKV_ERR_ALIGN;
+  return decode_entry(cache, k_pool, v_pool, page_table, q, num_q_heads, nullptr, nullptr,
+                      batch_idx, seq_lens, batch, scale, out, lse, workspace, workspace_bytes,
+                      dev_err, stream);
+}
 
-  CUtensorMap kmap, vmap;
-  st = encode_pool_map(&kmap, k_pool, cache);
-  if (st != PKV_OK) return st;
-  st = encode_pool_map(&vmap, v_pool, cache);
-  if (st != PKV_OK) return st;
-
-  pkv::DecodeParams p;
-  p.q = q;
-  p.page_table = page_table;
-  p.batch_idx = batch_idx;
-  p.seq_lens = seq_lens;
-  p.out = out;
-  p.lse = lse;
-  p.partials = static_cast<float*>(workspace);
-  p.dev_err = dev_err;
-  p.batch = batch;
-  p.num_q_heads = num_q_heads;
-  p.num_kv_heads = cache->num_kv_heads;
-  p.page_size = cache->page_size;
-  p.num_pages = cache->num_pages;
-  p.max_batch = cache->max_batch;
-  p.max_blocks = cache->max_blocks;
-  p.num_workers = workers;
-  p.qscale = scale * 1.4426950408889634f;
-  return cuda_status(pkv::launch_decode(p, kmap, vmap, sms, stream));
+pkv_status pkv_decode_append_attention(const pkv_cache_desc* cache, void* k_pool, void* v_pool,
+                                       const int32_t* page_table, const void* q,
+                                       int num_q_heads, const void* k_new, const void* v_new,
+                                       const int32_t* batch_idx, const int32_t* seq_lens,
+                                       int batch, float scale, void* out, float* lse,
+                                       void* workspace, size_t workspace_bytes,
+                                       int32_t* dev_err, cudaStream_t stream) {
+  if (batch > 0 && (k_new == nullptr || v_new == nullptr)) return PKV_ERR_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16)) return PKV_ERR_ALIGN;
+  return decode_entry(cache, k_pool, v_pool, page_table, q, num_q_heads, k_new, v_new,
+                      batch_idx, seq_lens, batch, scale, out, lse, workspace, workspace_bytes,
+                      dev_err, stream);
 }
 
 pkv_status pkv_prefill_attention(const void* q, const void* k, const void* v, int num_q_heads,

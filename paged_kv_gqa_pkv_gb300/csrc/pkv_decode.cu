@@ -139,6 +139,29 @@ __device__ __forceinline__ void rs_step(float* v, int lane, int& idx0) {
   if (upper) idx0 += H;
 }
 
+// Fused append: the new token of item (b, kvh), at position seq_lens[b] - 1,
+// copied from k_new/v_new into the pools (lanes 0-15 a K chunk of 16 bytes,
+// lanes 16-31 a V chunk). Only the warp that reads the item's last tile
+// calls this, before its own TMA read of that tile.
+__device__ __forceinline__ void append_new_token(const DecodeParams& p, const int32_t* s_slot,
+                                                 const int32_t* s_len, int b, int kvh, int lane) {
+  const int n = s_len[b];
+  const int pos = n - 1;
+  const int hkv = p.num_kv_heads;
+  const int64_t src = (static_cast<int64_t>(b) * hkv + kvh) * kHeadDim + (lane & 15) * 8;
+  const uint4 val = *reinterpret_cast<const uint4*>(
+      static_cast<const __nv_bfloat16*>(lane < 16 ? p.k_new : p.v_new) + src);
+  const int page = p.page_table[static_cast<int64_t>(s_slot[b]) * p.max_blocks + pos / p.page_size];
+  if (page < 0 || page >= p.num_pages) {
+    if (lane == 0) set_dev_err(p.dev_err, PKV_DEV_ERR_BAD_PAGE);
+    return;
+  }
+  const int64_t row = static_cast<int64_t>(page) * p.page_size + pos % p.page_size;
+  const int64_t dst = (row * hkv + kvh) * kHeadDim + (lane & 15) * 8;
+  *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(lane < 16 ? p.k_pool : p.v_pool) + dst) =
+      val;
+}
+
 // Producer-side view of the current row's pages (warp-uniform).
 struct RowPages {
   int b;            // row these describe (-1: none yet)
@@ -274,10 +297,8 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
       const int row = page * p.page_size + t0 % p.page_size;
       const bool seg_start = (k == 0) || (c.tile == 0);
       mbar_arrive_expect_tx(&bars[s], 2 * kKTileBytes + (seg_start ? C::kQBytes : 0));
-      tma_load_3d(st, &kmap, &bars[s], 0, c.kvh, row);
-      tma_load_3d(st + kHalfBytes, &kmap, &bars[s], 64, c.kvh, row);
-      tma_load_3d(st + C::kOffV, &vmap, &bars[s], 0, c.kvh, row);
-      tma_load_3d(st + C::kOffV + kHalfBytes, &vmap, &bars[s], 64, c.kvh, row);
+      tma_load_4d(st, &kmap, &bars[s], 0, row, 0, c.kvh);
+      tma_load_4d(st + C::kOffV, &vmap, &bars[s], 0, row, 0, c.kvh);
       if (seg_start) {
         const size_t qoff =
             (static_cast<size_t>(c.b) * p.num_q_heads + static_cast<size_t>(c.kvh) * G) *
@@ -289,6 +310,23 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
 
   load_row_pages(rp, p, s_slot, start.b, start.tiles, lane);
   pdl_wait_primary();
+  if (p.k_new != nullptr) {
+    // Fused append: this warp owns the new tokens of the items whose last
+    // tile lies in its range. They reach the pools before any TMA read here.
+    Cursor c = start;
+    int64_t u = u_begin;
+    while (true) {
+      const int64_t u_last = u + (c.tiles - 1 - c.tile);
+      if (u_last >= u_end) break;
+      append_new_token(p, s_slot, s_len, c.b, c.kvh, lane);
+      u = u_last + 1;
+      if (u >= u_end) break;
+      c.tile = c.tiles - 1;
+      advance(c, s_prefix, hkv);
+    }
+    fence_proxy_async_global();
+    __syncwarp();
+  }
   const int prologue = min(S, count);
   for (int k = 0; k < prologue; ++k) {
     issue(pc, k);

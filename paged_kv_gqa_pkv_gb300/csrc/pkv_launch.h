@@ -52,6 +52,12 @@ struct DecodeParams {
   void* out;                  // bf16 [B, Hq, D]
   float* lse;                 // [B, Hq]
   float* partials;            // workspace: (num_workers + B*Hkv) slots
+  // Fused append (all null for attention alone): the new token of row b,
+  // k_new/v_new bf16 [B, Hkv, D], goes to position seq_lens[b] - 1 of its slot.
+  const void* k_new;
+  const void* v_new;
+  void* k_pool;               // the pools as written (the tensor maps read them)
+  void* v_pool;
   int32_t* dev_err;
   int batch;
   int num_q_heads;

@@ -1,5 +1,6 @@
 """Bucketed CUDA-graph decode: append + split-KV decode captured once per
-batch-size bucket and replayed.
+batch-size bucket and replayed (by default as the fused append + decode
+call, two kernels a step; ``fused=False`` captures the separate append).
 
 This follows the pages' engine: one CUDA graph per batch-size bucket, decode
 dispatched to the smallest bucket that fits, and the unused rows of the
@@ -36,12 +37,17 @@ class DecodeGraphs:
         num_q_heads: query heads per row.
         scale: softmax scale.
         buckets: batch sizes to capture, ascending.
+        fused: capture ``pkv_decode_append_attention`` (the new token is
+            written at ``seq_lens - 1``, so ``input_pos`` must equal
+            ``seq_lens - 1`` on live rows) instead of ``pkv_append`` followed by
+            ``pkv_decode_attention``.
     """
 
     def __init__(self, k_pool, v_pool, page_table, page_size: int, num_q_heads: int,
-                 scale: float, buckets=DEFAULT_BUCKETS):
+                 scale: float, buckets=DEFAULT_BUCKETS, fused: bool = True):
         self.k_pool, self.v_pool, self.page_table = k_pool, v_pool, page_table
         self.page_size, self.scale = page_size, float(scale)
+        self.fused = bool(fused)
         self.buckets = tuple(sorted(int(b) for b in buckets))
         if not self.buckets or self.buckets[0] < 1:
             raise ValueError("buckets must be positive batch sizes")
@@ -72,6 +78,13 @@ class DecodeGraphs:
         torch.cuda.synchronize()
 
     def _launch(self, b: int) -> None:
+        if self.fused:
+            binding.pkv_decode_append_attention(
+                self.k_pool, self.v_pool, self.page_table, self.q[:b], self.k_new[:b],
+                self.v_new[:b], self.batch_idx[:b], self.seq_lens[:b], self.page_size,
+                self.scale, out=self.out[:b], lse=self.lse[:b], workspace=self.workspace,
+                dev_err=self.dev_err)
+            return
         binding.pkv_append(self.k_pool, self.v_pool, self.page_table, self.k_new[:b],
                            self.v_new[:b], self.batch_idx[:b], self.input_pos[:b],
                            self.page_size, dev_err=self.dev_err)

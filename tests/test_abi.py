@@ -128,3 +128,15 @@ def test_append_rope_rejects_bad_arguments(lib):
     assert lib.pkv_append_rope(*args(sin=264)) == 2
     assert lib.pkv_append_rope(*args(n=-1)) == 1
     assert lib.pkv_append_rope(*args(n=0)) == 0
+
+
+def test_decode_append_rejects_bad_arguments(lib):
+    d = _desc()
+    args = lambda kn=256, vn=256, hq=8, batch=4: (  # noqa: E731
+        ctypes.byref(d), P(256), P(256), P(256), P(256), hq, P(kn), P(vn), P(256), P(256),
+        batch, ctypes.c_float(0.088), P(256), P(256), P(256), 1 << 20, None, None)
+    assert lib.pkv_decode_append_attention(*args(kn=0)) == 1
+    assert lib.pkv_decode_append_attention(*args(vn=0)) == 1
+    assert lib.pkv_decode_append_attention(*args(kn=264)) == 2
+    assert lib.pkv_decode_append_attention(*args(hq=6)) == 1
+    assert lib.pkv_decode_append_attention(*args(batch=0, kn=0, vn=0)) == 0

@@ -20,12 +20,13 @@ def _rows(case, B):
             gpu(case.batch_idx[:B]), gpu(case.input_pos[:B]), gpu(case.seq_lens[:B]))
 
 
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "two_calls"])
 @pytest.mark.parametrize("B", [1, 3, 17, 64])
-def test_graph_replay_matches_eager(B):
+def test_graph_replay_matches_eager(B, fused):
     case = W.qwen3_b64_decode(0, permute=True)
     kp_g, vp_g, pt = gpu(case.k_pool), gpu(case.v_pool), gpu(case.page_table)
     graphs = DecodeGraphs(kp_g, vp_g, pt, case.page_size, case.num_q_heads, case.scale,
-                          buckets=(1, 2, 4, 8, 16, 32, 64))
+                          buckets=(1, 2, 4, 8, 16, 32, 64), fused=fused)
     q, kn, vn, bi, ip, sl = _rows(case, B)
     out_g, lse_g = graphs.step(q, kn, vn, bi, ip, sl)
     torch.cuda.synchronize()
@@ -40,14 +41,15 @@ def test_graph_replay_matches_eager(B):
     assert torch.equal(out_g, out_e) and torch.equal(lse_g, lse_e)
 
 
-def test_graph_steps_follow_the_cache_and_match_the_oracle():
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "two_calls"])
+def test_graph_steps_follow_the_cache_and_match_the_oracle(fused):
     """Two steps through one captured graph: the second sees the first step's
     appended tokens (the pools are updated in place, by pointer)."""
     case = W.custom_decode(4, [40, 130, 7, 300, 77], hq=32, hkv=8, page_size=128,
                            permute=True, max_blocks=4)
     kp, vp, pt = gpu(case.k_pool), gpu(case.v_pool), gpu(case.page_table)
     graphs = DecodeGraphs(kp, vp, pt, case.page_size, case.num_q_heads, case.scale,
-                          buckets=(4, 8))
+                          buckets=(4, 8), fused=fused)
     q, kn, vn, bi, ip, sl = _rows(case, case.batch)
     graphs.step(q, kn, vn, bi, ip, sl)
     # step 2: one more token per row
