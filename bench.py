@@ -57,17 +57,29 @@ def _peaks():
 
 def captured_traffic(key: str):
     """DRAM bytes per call from the committed ncu capture (profiles/traffic.json),
-    or None when the kernel source has changed since that capture."""
+    or None when any source the kernels are built from has changed since that
+    capture (sha256 over the listed sources, in order)."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)[key]
-        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != rec["source_sha256"]:
-                return None
+        m = hashlib.sha256()
+        for src in rec["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                m.update(f.read())
+        if m.hexdigest() != rec["sources_sha256"]:
+            return None
         return int(rec["dram_bytes_per_call"])
     except Exception:
         return None
+
+
+def step_bytes(case) -> int:
+    """Algorithmic bytes of one fused decode step: the decode launch's bytes
+    plus the append's (each live row's new K and V read once and written
+    once into the pool)."""
+    live = int((case.batch_idx != 0).sum())
+    return decode_bytes(case) + live * case.num_kv_heads * case.head_dim * 2 * 2 * 2
 
 
 def decode_bytes(case) -> int:
@@ -453,7 +465,8 @@ def run_pkv(args):
             dist.destroy_process_group()
         return
 
-    achieved = bytes_dec / (r["dec_ms"] * 1e-3) / 1e9
+    achieved = step_bytes(case) / (ms_step * 1e-3) / 1e9
+    dec_gbs = bytes_dec / (r["dec_ms"] * 1e-3) / 1e9
     perm = W.qwen3_b64_decode(0, permute=True)
     rp = timed_decode(perm, max(args.steps // 4, 10), args.warmup)
     e2e_ms, h2d, d2h = e2e_decode(case, max(args.steps // 10, 10), args.warmup)
@@ -469,13 +482,16 @@ def run_pkv(args):
         "tokens_per_s_per_layer": world * case.batch / (ms_step * 1e-3),
         "decode_call_us": r["dec_ms"] * 1e3, "decode_call_us_p10_p90": [r["dec_p10"] * 1e3,
                                                                          r["dec_p90"] * 1e3],
+        "decode_call_gbs": dec_gbs, "decode_call_frac": dec_gbs / hbm_peak,
         "two_call_step_us": r["two_call_ms"] * 1e3,
         "timing": f"CUDA-graph replay of {r['per_graph']}-step graphs; decode call = replay "
                   f"of {r['per_graph']} decode calls / {r['per_graph']}",
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": captured_traffic("decode_call"),
-                     "traffic_unit": "bytes per decode call (ncu dram read+write)",
-                     "kernel": "pkv_decode_attention (split-KV pass + LSE merge)",
+                     "frac": achieved / hbm_peak, "traffic": captured_traffic("decode_step"),
+                     "traffic_unit": "bytes per step (ncu dram read+write, both kernels)",
+                     "kernel": "pkv_decode_append_attention (split-KV pass with the fused "
+                               "append, then the LSE merge): the timed step",
+                     "algorithmic_bytes": step_bytes(case),
                      "peak_kind": peak_kind, "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS},
         "permuted_pages": {"decode_call_us": rp["dec_ms"] * 1e3,
                            "achieved_gbs": decode_bytes(perm) / (rp["dec_ms"] * 1e-3) / 1e9,
