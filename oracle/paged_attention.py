@@ -28,10 +28,17 @@ What the method computes (sources are the pages' own titles and sections):
   ("flex_vs_vllm.md", "What broke correctness and had to be dropped",
   ROWS_GUARANTEED_SAFE).
 
+* Before the cache write, k goes through the model's per-head ``k_norm`` and
+  the rotate-half rotary embedding ("qwen3_flex_inference.py", attention
+  ``forward`` and ``_apply_rotary``).
+
 Readings where the pages are silent (each is listed in the design notes):
 the LSE is the natural log of sum_t exp(scale * q.k_t); the q head h reads
 kv head h // (H_q / H_kv); rows of batch slot 0 or with no keys give
-out = 0 and lse = -inf; an append whose batch slot is 0 is skipped.
+out = 0 and lse = -inf; an append whose batch slot is 0 is skipped;
+``k_norm`` is the Qwen3 family's RMSNorm over the head dims (the pages name
+the module, not its formula), and normalisation and rotation are exact with
+one rounding to bf16 at the end.
 
 Representation: bf16 tensors are numpy ``uint16`` arrays of raw bf16 bit
 patterns; every arithmetic step is float64. Results are float64; callers that
@@ -147,6 +154,25 @@ def append(k_pool: np.ndarray, v_pool: np.ndarray, page_table: np.ndarray,
     return k_out, v_out, bad
 
 
+def k_norm(x: np.ndarray, weight: np.ndarray, eps: float) -> np.ndarray:
+    """Per-head RMS normalisation of K, the step the model applies to each
+    head of k just before the rotary embedding ("qwen3_flex_inference.py",
+    attention ``forward``: ``k = self.k_norm(self.k_proj(...).view(...,
+    head_dim))``, then ``_apply_rotary``). The pages name the module only; its
+    formula is the Qwen3 family's RMSNorm over the head dims with a learned
+    per-dim weight:
+    ``out[d] = weight[d] * x[d] / sqrt(mean over d' of x[d']**2 + eps)``.
+
+    ``x`` is bf16 bits ``[N, H, D]``, ``weight`` ``[D]`` (any float type).
+    Returns float64, unrounded: the rotation that follows works on the exact
+    value and the result is rounded to bf16 once, at the end.
+    """
+    xf = bf16_bits_to_f64(x)
+    w = np.asarray(weight, dtype=np.float64)
+    ms = np.mean(xf * xf, axis=-1, keepdims=True)
+    return w * (xf / np.sqrt(ms + float(eps)))
+
+
 def rope(x: np.ndarray, positions: np.ndarray, cos_table: np.ndarray,
          sin_table: np.ndarray) -> np.ndarray:
     """Rotary position embedding in the rotate-half form the pages apply to q
@@ -159,7 +185,12 @@ def rope(x: np.ndarray, positions: np.ndarray, cos_table: np.ndarray,
     ``x1 = x[:D/2]``, ``x2 = x[D/2:]``, ``c = cos[p]``, ``s = sin[p]``:
     ``out1 = x1*c - x2*s`` and ``out2 = x2*c + x1*s``. Returns float64.
     """
-    xf = bf16_bits_to_f64(x)
+    return rope_f64(bf16_bits_to_f64(x), positions, cos_table, sin_table)
+
+
+def rope_f64(xf: np.ndarray, positions: np.ndarray, cos_table: np.ndarray,
+             sin_table: np.ndarray) -> np.ndarray:
+    """``rope`` on float64 input ``[N, H, D]`` (e.g. the output of ``k_norm``)."""
     half = xf.shape[-1] // 2
     c = np.asarray(cos_table, dtype=np.float64)[np.asarray(positions, dtype=np.int64)]
     s = np.asarray(sin_table, dtype=np.float64)[np.asarray(positions, dtype=np.int64)]
@@ -172,18 +203,24 @@ def rope(x: np.ndarray, positions: np.ndarray, cos_table: np.ndarray,
 def append_rope(k_pool: np.ndarray, v_pool: np.ndarray, page_table: np.ndarray,
                 k_new: np.ndarray, v_new: np.ndarray, batch_idx: np.ndarray,
                 input_pos: np.ndarray, page_size: int, cos_table: np.ndarray,
-                sin_table: np.ndarray):
+                sin_table: np.ndarray, k_norm_weight=None, k_norm_eps: float = 1e-6):
     """KV append with the rotary embedding applied to K first: K rows are
     ``rope(k_new)`` rounded to bf16 (nearest even), V rows are copied as
-    they are. A token whose position has no table row is reported and not
-    written. Returns ``(k_pool_out, v_pool_out, bad_tokens)``."""
+    they are. With ``k_norm_weight`` given, K is first normalised per head
+    (``k_norm``) and the rotation acts on the exact normalised value: K rows
+    are ``rope(k_norm(k_new))`` rounded to bf16 once. A token whose position
+    has no table row is reported and not written. Returns
+    ``(k_pool_out, v_pool_out, bad_tokens)``."""
     n = len(batch_idx)
     pos = np.asarray(input_pos, dtype=np.int64)
     in_table = (pos >= 0) & (pos < len(cos_table))
     k_rot = np.array(k_new, dtype=np.uint16, copy=True)
     if in_table.any():
-        k_rot[in_table] = f64_to_bf16_bits(
-            rope(k_new[in_table], pos[in_table], cos_table, sin_table))
+        if k_norm_weight is None:
+            kf = bf16_bits_to_f64(k_new[in_table])
+        else:
+            kf = k_norm(k_new[in_table], k_norm_weight, k_norm_eps)
+        k_rot[in_table] = f64_to_bf16_bits(rope_f64(kf, pos[in_table], cos_table, sin_table))
     keep = [i for i in range(n) if in_table[i] or int(batch_idx[i]) == 0]
     k_out, v_out, bad = append(k_pool, v_pool, page_table, k_rot[keep], v_new[keep],
                                np.asarray(batch_idx)[keep], pos[keep], page_size)

@@ -463,3 +463,89 @@ def check_append_rope(orc):
 
 
 ALL_CHECKS += [check_rope_closed_forms, check_rope_relative_position, check_append_rope]
+
+
+# -------------------------------------------------------------- k_norm ----
+
+def check_k_norm_closed_forms(orc):
+    # x = (3, 4, 0, ..., 0): mean of squares 25/D, so out = w * x * sqrt(D) / 5
+    x = np.zeros((1, 1, D), dtype=np.float32)
+    x[0, 0, 0], x[0, 0, 1] = 3.0, 4.0
+    xb = _bits(torch.from_numpy(x).to(torch.bfloat16))
+    w = np.linspace(0.5, 1.5, D)
+    r = orc.k_norm(xb, w, 0.0)
+    want = np.zeros(D)
+    want[0], want[1] = 3.0 * w[0] * math.sqrt(D) / 5.0, 4.0 * w[1] * math.sqrt(D) / 5.0
+    assert np.allclose(r[0, 0], want, rtol=1e-15, atol=0)
+    # a constant head a: out = w * a / sqrt(a^2 + eps), eps included
+    a, eps = 0.375, 0.5
+    xc = _bits(torch.full((2, 3, D), a).to(torch.bfloat16))
+    rc = orc.k_norm(xc, w, eps)
+    assert np.allclose(rc, np.broadcast_to(w * a / math.sqrt(a * a + eps), rc.shape),
+                       rtol=1e-15, atol=0)
+    # all-zero head with eps > 0: zeros, not NaN
+    z = orc.k_norm(np.zeros((1, 2, D), dtype=np.uint16), w, 1e-6)
+    assert np.array_equal(z, np.zeros((1, 2, D)))
+
+
+def check_k_norm_invariants(orc):
+    gen = torch.Generator().manual_seed(61)
+    x = _bits(_rand_bf16(gen, (5, 4, D)))
+    # unit weight, eps 0: every head comes out with root-mean-square exactly 1
+    r = orc.k_norm(x, np.ones(D), 0.0)
+    assert np.allclose(np.sqrt(np.mean(r * r, axis=-1)), 1.0, rtol=1e-14)
+    # scaling a head by a power of two (exact in bf16) leaves it unchanged at eps 0
+    x2 = _bits(torch.from_numpy(orc.bf16_bits_to_f64(x) * 2.0).to(torch.bfloat16))
+    w = np.random.default_rng(3).uniform(0.5, 1.5, D)
+    assert np.array_equal(orc.k_norm(x2, w, 0.0), orc.k_norm(x, w, 0.0))
+    # the weight multiplies its own dim: two weights differing in one dim
+    # change that dim only
+    w2 = w.copy()
+    w2[77] *= 3.0
+    d = orc.k_norm(x, w2, 1e-6) - orc.k_norm(x, w, 1e-6)
+    assert np.count_nonzero(d[..., np.arange(D) != 77]) == 0
+    assert np.count_nonzero(d[..., 77]) == d[..., 77].size
+
+
+def check_append_rope_k_norm(orc):
+    """append_rope with k_norm against the same arithmetic written another
+    way: the norm through np.linalg.norm, the rotation as complex
+    multiplication (x1 + i x2) * exp(i theta), one rounding at the end."""
+    gen = torch.Generator().manual_seed(67)
+    ps, P, hkv = 16, 10, 2
+    from paged_kv_gqa_pkv_gb300.workloads import rope_tables
+    cos_t, sin_t = rope_tables(40)
+    kp = _bits(_rand_bf16(gen, (P * ps, hkv, D)))
+    vp = _bits(_rand_bf16(gen, (P * ps, hkv, D)))
+    table = np.full((3, 4), -1, dtype=np.int32)
+    table[1, :2] = [3, 5]
+    table[2, :3] = [7, 1, 2]
+    bidx = np.array([1, 2, 0, 2], dtype=np.int32)
+    pos = np.array([0, 33, 3, 39], dtype=np.int32)
+    kn = _bits(_rand_bf16(gen, (4, hkv, D)) * 3.0)
+    vn = _bits(_rand_bf16(gen, (4, hkv, D)))
+    w = np.random.default_rng(5).uniform(0.25, 2.0, D)   # not symmetric in d, d + D/2
+    eps = 1e-6
+    ko, vo, bad = orc.append_rope(kp, vp, table, kn, vn, bidx, pos, ps, cos_t.numpy(),
+                                  sin_t.numpy(), k_norm_weight=w, k_norm_eps=eps)
+    assert bad == []
+    half = D // 2
+    for i, row in [(0, 3 * ps + 0), (1, 2 * ps + 33 % ps), (3, 2 * ps + 39 % ps)]:
+        xf = orc.bf16_bits_to_f64(kn[i])                       # [hkv, D]
+        rms = np.linalg.norm(xf, axis=-1, keepdims=True) / math.sqrt(D)
+        y = w * xf / np.sqrt(rms * rms + eps)
+        theta = np.arctan2(sin_t.numpy()[pos[i]].astype(np.float64),
+                           cos_t.numpy()[pos[i]].astype(np.float64))
+        mag = np.hypot(sin_t.numpy()[pos[i]].astype(np.float64),
+                       cos_t.numpy()[pos[i]].astype(np.float64))
+        zc = (y[:, :half] + 1j * y[:, half:]) * (mag * np.exp(1j * theta))
+        want = np.concatenate([zc.real, zc.imag], axis=-1)
+        got = orc.bf16_bits_to_f64(ko[row])
+        ulp = np.abs(np.asarray(want)) * 2.0 ** -8 + 1e-30
+        assert np.all(np.abs(got - want) <= ulp)
+        assert np.array_equal(vo[row], vn[i])
+    # position 0 rotates by nothing: the row is k_norm(k) rounded once
+    assert np.array_equal(ko[3 * ps], orc.f64_to_bf16_bits(orc.k_norm(kn[0:1], w, eps))[0])
+
+
+ALL_CHECKS += [check_k_norm_closed_forms, check_k_norm_invariants, check_append_rope_k_norm]

@@ -182,7 +182,47 @@ def _append_rope_on_v(k_pool, v_pool, table, k_new, v_new, bidx, pos, ps, cos_t,
     return _real_append_rope(k_pool, v_pool, table, k_new, v_rot, bidx, pos, ps, cos_t, sin_t)
 
 
+def _k_norm_sum(x, weight, eps):
+    xf = orc.bf16_bits_to_f64(x)
+    return np.asarray(weight, dtype=np.float64) * xf / np.sqrt(
+        np.sum(xf * xf, axis=-1, keepdims=True) + eps)            # planted: sum, not mean
+
+
+def _k_norm_no_eps(x, weight, eps):
+    xf = orc.bf16_bits_to_f64(x)
+    ms = np.mean(xf * xf, axis=-1, keepdims=True)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        return np.asarray(weight, dtype=np.float64) * xf / np.sqrt(ms)   # planted: eps dropped
+
+
+def _k_norm_weight_reversed(x, weight, eps):
+    xf = orc.bf16_bits_to_f64(x)
+    ms = np.mean(xf * xf, axis=-1, keepdims=True)
+    return np.asarray(weight, dtype=np.float64)[::-1] * xf / np.sqrt(ms + eps)   # planted
+
+
+def _append_rope_norm_after(k_pool, v_pool, table, k_new, v_new, bidx, pos, ps, cos_t, sin_t,
+                            k_norm_weight=None, k_norm_eps=1e-6):
+    # planted: the rotation first, the normalisation (and its weight) after it
+    if k_norm_weight is None:
+        return _real_append_rope(k_pool, v_pool, table, k_new, v_new, bidx, pos, ps, cos_t,
+                                 sin_t)
+    posa = np.asarray(pos, dtype=np.int64)
+    ok = (posa >= 0) & (posa < len(cos_t))
+    k2 = np.array(k_new, copy=True)
+    r = orc.rope(k_new[ok], posa[ok], cos_t, sin_t)
+    ms = np.mean(r * r, axis=-1, keepdims=True)
+    k2[ok] = orc.f64_to_bf16_bits(np.asarray(k_norm_weight) * r / np.sqrt(ms + k_norm_eps))
+    zero = np.zeros_like(cos_t)
+    one = np.ones_like(cos_t)
+    return _real_append_rope(k_pool, v_pool, table, k2, v_new, bidx, pos, ps, one, zero)
+
+
 MUTANTS.update({
+    "k_norm_sum_not_mean": ("k_norm", _k_norm_sum),
+    "k_norm_drops_eps": ("k_norm", _k_norm_no_eps),
+    "k_norm_weight_reversed": ("k_norm", _k_norm_weight_reversed),
+    "append_rope_norm_after_rotation": ("append_rope", _append_rope_norm_after),
     "rope_sign_flipped": ("rope", _rope_sign_flipped),
     "rope_interleaved_pairs": ("rope", _rope_interleaved),
     "append_rope_rotates_v": ("append_rope", _append_rope_on_v),
