@@ -14,7 +14,8 @@
  * ("qwen3_flex_inference.py", attention forward, _decode_step_eager,
  * _prefill):
  *   pkv_append            - write new tokens' K/V rows through the page table
- *   pkv_append_rope       - the same with the rotary embedding applied to K
+ *   pkv_append_rope       - the same with k_norm and the rotary embedding
+ *                           applied to K
  *   pkv_decode_attention  - one query token per row, GQA, over the pages
  *   pkv_prefill_attention - packed document-causal attention over fresh k/v
  *
@@ -100,11 +101,12 @@ pkv_status pkv_append(const pkv_cache_desc* cache, void* k_pool, void* v_pool,
                       cudaStream_t stream);
 
 /*
- * pkv_append_rope - pkv_append with the rotary position embedding applied to
- * each new K row on the way into the pool (V rows are copied unchanged).
- * Source: "qwen3_flex_inference.py", _apply_rotary (x * cos + rotate_half(x)
- * * sin with rotate_half(x) = cat(-x2, x1), applied to k right before the
- * cache write in the attention forward).
+ * pkv_append_rope - pkv_append with the model's per-head k_norm (optional)
+ * and the rotary position embedding applied to each new K row on the way
+ * into the pool (V rows are copied unchanged).
+ * Source: "qwen3_flex_inference.py", attention forward (k = k_norm(k_proj(..)
+ * per head), then _apply_rotary: x * cos + rotate_half(x) * sin with
+ * rotate_half(x) = cat(-x2, x1), right before the cache write).
  *
  * rope_cos, rope_sin: fp32 [rope_len, D/2] row-major, 16-byte aligned; row p
  * holds the cos/sin of the angles of position p (the full-width tables repeat
@@ -112,6 +114,13 @@ pkv_status pkv_append(const pkv_cache_desc* cache, void* k_pool, void* v_pool,
  * p = input_pos[i], with x1 = k_new[i][h][0:D/2], x2 = k_new[i][h][D/2:D],
  * c = rope_cos[p], s = rope_sin[p]:
  *     K row = bf16_rne(concat(x1*c - x2*s, x2*c + x1*s))   (computed in fp32)
+ * k_norm_weight: null (no normalisation) or fp32 [D], 16-byte aligned. When
+ * given, each head x of k_new[i] is first replaced by
+ *     x_d * k_norm_weight[d] / sqrt(mean_d(x_d^2) + k_norm_eps)
+ * (the pages name the k_norm module; this is the Qwen3 family's RMSNorm over
+ * the head dims), kept in fp32 and rotated, with one rounding to bf16 at the
+ * end. k_norm_eps must be finite and >= 0 (else PKV_ERR_ARG); it is ignored
+ * without a weight.
  * A position outside [0, rope_len) sets PKV_DEV_ERR_BAD_POS and skips the
  * token; everything else (slots, pages, errors, races) is as pkv_append.
  */
@@ -120,6 +129,7 @@ pkv_status pkv_append_rope(const pkv_cache_desc* cache, void* k_pool, void* v_po
                            const void* v_new, const int32_t* batch_idx,
                            const int32_t* input_pos, int n_tokens,
                            const float* rope_cos, const float* rope_sin, int rope_len,
+                           const float* k_norm_weight, float k_norm_eps,
                            int32_t* dev_err, cudaStream_t stream);
 
 /*

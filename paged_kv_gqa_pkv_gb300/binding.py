@@ -72,7 +72,7 @@ def load_library() -> ctypes.CDLL:
     lib.pkv_append.argtypes = [desc_p, vp, vp, i32p, vp, vp, i32p, i32p, c_int, i32p, vp]
     lib.pkv_append.restype = c_int
     lib.pkv_append_rope.argtypes = [desc_p, vp, vp, i32p, vp, vp, i32p, i32p, c_int, f32p, f32p,
-                                    c_int, i32p, vp]
+                                    c_int, f32p, c_float, i32p, vp]
     lib.pkv_append_rope.restype = c_int
     lib.pkv_decode_workspace_size.argtypes = [desc_p, c_int, c_int, c_int]
     lib.pkv_decode_workspace_size.restype = c_size
@@ -158,9 +158,11 @@ def pkv_append(k_pool, v_pool, page_table, k_new, v_new, batch_idx, input_pos,
 
 
 def pkv_append_rope(k_pool, v_pool, page_table, k_new, v_new, batch_idx, input_pos,
-                    page_size: int, rope_cos, rope_sin, dev_err=None, stream=None) -> None:
-    """pkv_append with the rotary embedding applied to K; rope_cos/rope_sin are
-    fp32 [L, D/2] tables indexed by position."""
+                    page_size: int, rope_cos, rope_sin, k_norm_weight=None,
+                    k_norm_eps: float = 1e-6, dev_err=None, stream=None) -> None:
+    """pkv_append with the rotary embedding (and, given ``k_norm_weight``
+    fp32 [D], the per-head k_norm before it) applied to K; rope_cos/rope_sin
+    are fp32 [L, D/2] tables indexed by position."""
     for name, t, dt, nd in (("k_pool", k_pool, torch.bfloat16, 3),
                             ("v_pool", v_pool, torch.bfloat16, 3),
                             ("page_table", page_table, torch.int32, 2),
@@ -173,11 +175,16 @@ def pkv_append_rope(k_pool, v_pool, page_table, k_new, v_new, batch_idx, input_p
         _need(t, name, dt, nd)
     if rope_cos.shape != rope_sin.shape or rope_cos.shape[1] * 2 != k_new.shape[2]:
         raise ValueError("rope tables must both be [L, D/2]")
+    if k_norm_weight is not None:
+        _need(k_norm_weight, "k_norm_weight", torch.float32, 1)
+        if k_norm_weight.shape[0] != k_new.shape[2]:
+            raise ValueError("k_norm_weight must be [D]")
     desc = cache_desc(k_pool, page_table, page_size)
     st = load_library().pkv_append_rope(
         ctypes.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(k_new),
         _ptr(v_new), _ptr(batch_idx), _ptr(input_pos), int(batch_idx.numel()), _ptr(rope_cos),
-        _ptr(rope_sin), int(rope_cos.shape[0]), _ptr(dev_err), _stream(stream))
+        _ptr(rope_sin), int(rope_cos.shape[0]), _ptr(k_norm_weight), float(k_norm_eps),
+        _ptr(dev_err), _stream(stream))
     _check("pkv_append_rope", st)
 
 

@@ -248,17 +248,21 @@ pkv_status pkv_append_rope(const pkv_cache_desc* cache, void* k_pool, void* v_po
                            const int32_t* page_table, const void* k_new, const void* v_new,
                            const int32_t* batch_idx, const int32_t* input_pos, int n_tokens,
                            const float* rope_cos, const float* rope_sin, int rope_len,
-                           int32_t* dev_err, cudaStream_t stream) {
+                           const float* k_norm_weight, float k_norm_eps, int32_t* dev_err,
+                           cudaStream_t stream) {
   pkv_status st = check_cache(cache);
   if (st != PKV_OK) return st;
   if (n_tokens < 0 || rope_len <= 0) return PKV_ERR_ARG;
+  if (k_norm_weight != nullptr && !(k_norm_eps >= 0.f && k_norm_eps < INFINITY))
+    return PKV_ERR_ARG;
   if (n_tokens == 0) return PKV_OK;
   if (!k_pool || !v_pool || !page_table || !k_new || !v_new || !batch_idx || !input_pos ||
       !rope_cos || !rope_sin)
     return PKV_ERR_ARG;
   if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) ||
       !aligned(rope_cos, 16) || !aligned(rope_sin, 16) || !aligned(page_table, 4) ||
-      !aligned(batch_idx, 4) || !aligned(input_pos, 4) || !aligned(dev_err, 4))
+      !aligned(batch_idx, 4) || !aligned(input_pos, 4) || !aligned(dev_err, 4) ||
+      !aligned(k_norm_weight, 16))
     return PKV_ERR_ALIGN;
   int sms = 0;
   st = device_info(&sms);
@@ -282,6 +286,8 @@ pkv_status pkv_append_rope(const pkv_cache_desc* cache, void* k_pool, void* v_po
   p.rope_sin = rope_sin;
   p.rope_len = rope_len;
   p.num_kv_heads = cache->num_kv_heads;
+  p.k_norm_weight = k_norm_weight;
+  p.k_norm_eps = k_norm_eps;
   return cuda_status(pkv::launch_append_rope(p, stream));
 }
 

@@ -65,6 +65,10 @@ append_kernel(AppendParams p) {
 // A lane takes one 16-byte chunk of the first half of a head and its partner
 // chunk of the second half; the tables' eight cos and sin values of that
 // chunk are two float4 loads each. V rows are copied unchanged.
+// With a k_norm weight, K is first normalised per head (the model's k_norm,
+// applied to k just before _apply_rotary): x_d * w_d / sqrt(mean x^2 + eps).
+// The 8 lanes of a head (an aligned group of 8) add their sums of squares
+// with three shuffles, so the loop steps all lanes together.
 // a*c - b*s and a*c + b*s accurate to about one fp32 ulp of the result even
 // when the two products nearly cancel: the rounding error of b*s is kept
 // exactly (an FMA) and folded back in after the fused multiply-add.
@@ -115,25 +119,61 @@ append_rope_kernel(AppendRopeParams rp) {
   const float4* cs = reinterpret_cast<const float4*>(rp.rope_cos + static_cast<int64_t>(pos) * (kHeadDim / 2));
   const float4* sn = reinterpret_cast<const float4*>(rp.rope_sin + static_cast<int64_t>(pos) * (kHeadDim / 2));
   const int pairs = rp.num_kv_heads * 8;  // eight 16-byte chunk pairs per head
-  for (int e = lane; e < pairs; e += 32) {
+  const float* wn = rp.k_norm_weight;
+  for (int e0 = 0; e0 < pairs; e0 += 32) {
+    const int e = e0 + lane;
+    const bool act = e < pairs;  // whole groups of 8: pairs is a multiple of 8
     const int h = e >> 3;
     const int c = e & 7;
-    const uint4 a = __ldg(ks + h * 16 + c);
-    const uint4 bb = __ldg(ks + h * 16 + 8 + c);
+    uint4 a = make_uint4(0u, 0u, 0u, 0u), bb = a;
+    if (act) {
+      a = __ldg(ks + h * 16 + c);
+      bb = __ldg(ks + h * 16 + 8 + c);
+    }
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+    const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
+    float x1[8], x2[8];  // dims 8c..8c+7 and D/2 + 8c..
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      x1[2 * u] = bf16lo(aw[u]);
+      x1[2 * u + 1] = bf16hi(aw[u]);
+      x2[2 * u] = bf16lo(bw[u]);
+      x2[2 * u + 1] = bf16hi(bw[u]);
+    }
+    if (wn != nullptr) {
+      float ss = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ss = fmaf(x1[j], x1[j], fmaf(x2[j], x2[j], ss));
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+      const float inv = rsqrtf(ss * (1.f / kHeadDim) + rp.k_norm_eps);
+      if (act) {
+        const float4* w1 = reinterpret_cast<const float4*>(wn + 8 * c);
+        const float4* w2 = reinterpret_cast<const float4*>(wn + kHeadDim / 2 + 8 * c);
+        const float4 wa = __ldg(w1), wb = __ldg(w1 + 1), wc = __ldg(w2), wd = __ldg(w2 + 1);
+        const float wv1[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+        const float wv2[8] = {wc.x, wc.y, wc.z, wc.w, wd.x, wd.y, wd.z, wd.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          x1[j] = (x1[j] * inv) * wv1[j];
+          x2[j] = (x2[j] * inv) * wv2[j];
+        }
+      }
+    }
+    if (!act) continue;
     const float4 c0 = __ldg(cs + 2 * c), c1 = __ldg(cs + 2 * c + 1);
     const float4 s0 = __ldg(sn + 2 * c), s1 = __ldg(sn + 2 * c + 1);
     const float cv[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
     const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
-    const uint32_t bw[4] = {bb.x, bb.y, bb.z, bb.w};
     uint32_t o1[4], o2[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const float x1l = bf16lo(aw[u]), x1h = bf16hi(aw[u]);
-      const float x2l = bf16lo(bw[u]), x2h = bf16hi(bw[u]);
-      const float cl = cv[2 * u], ch = cv[2 * u + 1], sl = sv[2 * u], sh = sv[2 * u + 1];
-      o1[u] = pack_bf16x2(rot_diff(x1l, cl, x2l, sl), rot_diff(x1h, ch, x2h, sh));
-      o2[u] = pack_bf16x2(rot_sum(x2l, cl, x1l, sl), rot_sum(x2h, ch, x1h, sh));
+      const int l = 2 * u, hh = 2 * u + 1;
+      o1[u] = pack_bf16x2(rot_diff(x1[l], cv[l], x2[l], sv[l]),
+                          rot_diff(x1[hh], cv[hh], x2[hh], sv[hh]));
+      o2[u] = pack_bf16x2(rot_sum(x2[l], cv[l], x1[l], sv[l]),
+                          rot_sum(x2[hh], cv[hh], x1[hh], sv[hh]));
     }
     kd[h * 16 + c] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
     kd[h * 16 + 8 + c] = make_uint4(o2[0], o2[1], o2[2], o2[3]);

@@ -39,6 +39,8 @@ struct AppendRopeParams {
   const float* rope_sin;
   int rope_len;
   int num_kv_heads;
+  const float* k_norm_weight;  // [D] or null: no k_norm
+  float k_norm_eps;
 };
 
 // Split-KV decode. The work of a call is the sequence of 16-token tiles of all

@@ -120,10 +120,13 @@ def test_without_a_gpu_calls_fail_cleanly(lib):
 
 def test_append_rope_rejects_bad_arguments(lib):
     d = _desc()
-    args = lambda cos=256, sin=256, n=4, L=32: (  # noqa: E731
+    args = lambda cos=256, sin=256, n=4, L=32, w=0, eps=1e-6: (  # noqa: E731
         ctypes.byref(d), P(256), P(256), P(256), P(256), P(256), P(256), P(256), n, P(cos),
-        P(sin), L, None, None)
+        P(sin), L, P(w) if w else None, ctypes.c_float(eps), None, None)
     assert lib.pkv_append_rope(*args(cos=0)) == 1
+    assert lib.pkv_append_rope(*args(w=256, eps=-1.0)) == 1
+    assert lib.pkv_append_rope(*args(w=256, eps=float("nan"))) == 1
+    assert lib.pkv_append_rope(*args(w=264)) == 2
     assert lib.pkv_append_rope(*args(L=0)) == 1
     assert lib.pkv_append_rope(*args(sin=264)) == 2
     assert lib.pkv_append_rope(*args(n=-1)) == 1
