@@ -315,6 +315,51 @@ def decode_attention(q: np.ndarray, k_pool: np.ndarray, v_pool: np.ndarray,
     return out, lse, bad
 
 
+def paged_prefill_attention(q: np.ndarray, k_pool: np.ndarray, v_pool: np.ndarray,
+                            page_table: np.ndarray, batch_idx: np.ndarray,
+                            input_pos: np.ndarray, page_size: int, scale: float, rows=None):
+    """Chunked prefill over the paged cache: packed query token i (``q[i]``,
+    ``[H_q, D]`` bf16 bits) attends the logical keys ``0..input_pos[i]`` of its
+    batch slot ``batch_idx[i]``, read through the page table, the token's own
+    chunk included (its K/V were appended first). This is the step the pages
+    leave on the table: prefill that reads its earlier context from the pages,
+    so that prefill chunks and decode tokens can share one pass
+    ("flex_vs_vllm.md", "What's left on the table", chunked prefill; the
+    prefill there reads the packed fresh k/v instead,
+    "qwen3_flex_inference.py", ``_prefill``). The rule per token is the
+    decode rule (``_decode_block_mask``, ``causal_offset``: ``kv_idx <=
+    input_pos``); tokens need no particular order or packing.
+
+    Tokens of slot 0 give out 0, lse -inf. Tokens whose keys cannot all be
+    addressed (a position past the table, an unreserved entry) are NaN and
+    listed in the returned ``bad_rows``. ``rows`` optionally restricts the
+    computation to some tokens (the others stay NaN).
+
+    Returns ``(out [T, H_q, D], lse [T, H_q], bad_rows)`` in float64.
+    """
+    T, hq, d = q.shape
+    out = np.full((T, hq, d), np.nan)
+    lse = np.full((T, hq), np.nan)
+    bad = []
+    for i in (range(T) if rows is None else rows):
+        slot = int(batch_idx[i])
+        if slot == 0:
+            out[i] = 0.0
+            lse[i] = -np.inf
+            continue
+        n = int(input_pos[i]) + 1
+        if n <= 0:
+            bad.append(i)
+            continue
+        K = gather_logical(k_pool, page_table, slot, n, page_size)
+        V = gather_logical(v_pool, page_table, slot, n, page_size)
+        if K is None or V is None:
+            bad.append(i)
+            continue
+        out[i], lse[i] = attend(bf16_bits_to_f64(q[i]), K, V, scale)
+    return out, lse, bad
+
+
 def prefill_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray,
                       batch_idx: np.ndarray, input_pos: np.ndarray,
                       scale: float, rows=None):

@@ -91,6 +91,39 @@ class PrefillCase:
         return int(self.q.shape[0])
 
 
+@dataclass
+class ChunkedCase:
+    """Inputs of one chunked-prefill step over the paged cache: each sequence
+    already holds a prefix in the pools and brings a chunk of new tokens (a
+    decode token is a chunk of one); the chunk's K/V are appended, then every
+    packed query token attends its slot's keys 0..input_pos through the
+    pages."""
+    name: str
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    num_pages: int
+    max_batch: int
+    max_blocks: int
+    scale: float
+    q: torch.Tensor             # bf16 [T, Hq, D]
+    k_new: torch.Tensor         # bf16 [T, Hkv, D] (the chunks' own K/V)
+    v_new: torch.Tensor
+    batch_idx: torch.Tensor     # int32 [T]
+    input_pos: torch.Tensor     # int32 [T]
+    prefix_lens: list           # per slot 1.., tokens already in the pools
+    chunk_lens: list            # per slot 1.., new tokens in this step
+    k_pool: torch.Tensor        # bf16 [P*ps, Hkv, D], prefixes filled
+    v_pool: torch.Tensor
+    page_table: torch.Tensor
+    info: dict = field(default_factory=dict)
+
+    @property
+    def n_tokens(self) -> int:
+        return int(self.q.shape[0])
+
+
 def _randn_bf16(shape, gen) -> torch.Tensor:
     return torch.randn(shape, generator=gen, dtype=torch.float32).to(torch.bfloat16)
 
@@ -266,6 +299,70 @@ def packed_prefill(seed: int = 0, n_docs: int = 64, lo: int = 64,
         info={"tokens": T, "pairs": int(sum(n * (n + 1) // 2 for n in doc_lens))})
 
 
+def chunked_prefill(seed: int = 0, *, prefix_lens=None, chunk_lens=None, n_chunks: int = 16,
+                    chunk: int = 512, prefix_lo: int = 512, prefix_hi: int = 4096,
+                    n_decode: int = 48, decode_lo: int = 512, decode_hi: int = 2048,
+                    hq: int = 32, hkv: int = 8, page_size: int = 128, permute: bool = True,
+                    shuffle: bool = True, n_pad: int = 0, fill=None) -> ChunkedCase:
+    """One mixed step of chunked prefill, the pages' missing piece (prefill
+    and decode in one pass; "flex_vs_vllm.md", "What's left on the table"):
+    ``n_chunks`` sequences with a prefix of U[prefix_lo, prefix_hi] tokens in
+    the cache bring ``chunk`` new tokens each, and ``n_decode`` sequences with
+    a prefix of U[decode_lo, decode_hi] bring one. ``prefix_lens`` and
+    ``chunk_lens`` (per slot) override the draw. Each sequence's chunk is
+    contiguous in the packed order; the sequences come in a seeded random
+    order (``shuffle``) and ``n_pad`` padding tokens (slot 0) trail them. The
+    pools hold random prefixes; rows past a sequence's prefix hold random
+    values, or ``fill`` when given (e.g. NaN)."""
+    gen = torch.Generator().manual_seed(seed)
+    if prefix_lens is None:
+        pre = torch.randint(prefix_lo, prefix_hi + 1, (n_chunks,), generator=gen).tolist()
+        pre += torch.randint(decode_lo, decode_hi + 1, (n_decode,), generator=gen).tolist()
+        chunk_lens = [chunk] * n_chunks + [1] * n_decode
+    else:
+        pre = list(prefix_lens)
+        chunk_lens = list(chunk_lens)
+    pre = [int(x) for x in pre]
+    chunk_lens = [int(x) for x in chunk_lens]
+    S = len(pre)
+    d = HEAD_DIM
+    blocks = [_blocks(p + c, page_size) for p, c in zip(pre, chunk_lens)]
+    max_blocks = max(blocks) if blocks else 1
+    num_pages = 1 + sum(blocks)
+    table = assign_pages(blocks, num_pages, S + 1, max_blocks, gen, permute)
+    rows = num_pages * page_size
+    if fill is None:
+        k_pool = _randn_bf16((rows, hkv, d), gen)
+        v_pool = _randn_bf16((rows, hkv, d), gen)
+    else:
+        k_pool = torch.full((rows, hkv, d), fill, dtype=torch.bfloat16)
+        v_pool = torch.full((rows, hkv, d), fill, dtype=torch.bfloat16)
+        for s in range(S):   # the prefixes are real data
+            for t in range(pre[s]):
+                r = int(table[s + 1, t // page_size]) * page_size + t % page_size
+                k_pool[r] = _randn_bf16((hkv, d), gen)
+                v_pool[r] = _randn_bf16((hkv, d), gen)
+    order = torch.randperm(S, generator=gen).tolist() if shuffle else list(range(S))
+    bidx, pos = [], []
+    for s in order:
+        bidx += [s + 1] * chunk_lens[s]
+        pos += list(range(pre[s], pre[s] + chunk_lens[s]))
+    bidx += [0] * n_pad
+    pos += [0] * n_pad
+    T = len(bidx)
+    q = _randn_bf16((T, hq, d), gen)
+    k_new = _randn_bf16((T, hkv, d), gen)
+    v_new = _randn_bf16((T, hkv, d), gen)
+    return ChunkedCase(
+        name=f"chunked_prefill_{S}seq_T{T}", num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+        page_size=page_size, num_pages=num_pages, max_batch=S + 1, max_blocks=max_blocks,
+        scale=1.0 / math.sqrt(d), q=q, k_new=k_new, v_new=v_new,
+        batch_idx=torch.tensor(bidx, dtype=torch.int32),
+        input_pos=torch.tensor(pos, dtype=torch.int32), prefix_lens=pre,
+        chunk_lens=chunk_lens, k_pool=k_pool, v_pool=v_pool, page_table=table,
+        info={"tokens": T, "pairs": int(sum((p + 1) for b, p in zip(bidx, pos) if b != 0))})
+
+
 def rope_tables(max_pos: int, head_dim: int = HEAD_DIM, theta: float = 1.0e6):
     """fp32 cos/sin tables ``[max_pos, head_dim/2]`` of the standard rotary
     embedding: angle ``p * theta**(-2i/head_dim)`` for row p, column i
@@ -283,6 +380,7 @@ WORKLOADS = {
     "padded_bucket_decode": padded_bucket_decode,
     "long_context_decode": long_context_decode,
     "packed_prefill": packed_prefill,
+    "chunked_prefill": chunked_prefill,
 }
 
 

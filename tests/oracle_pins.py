@@ -549,3 +549,111 @@ def check_append_rope_k_norm(orc):
 
 
 ALL_CHECKS += [check_k_norm_closed_forms, check_k_norm_invariants, check_append_rope_k_norm]
+
+
+# ---------------------------------------------------- paged (chunked) prefill --
+
+def _chunk_case(orc, prefix_lens, chunk_lens, page_size, seed, hq=8, hkv=2, shuffle=True,
+                n_pad=0):
+    from paged_kv_gqa_pkv_gb300 import workloads as W
+    c = W.chunked_prefill(seed, prefix_lens=prefix_lens, chunk_lens=chunk_lens, hq=hq, hkv=hkv,
+                          page_size=page_size, shuffle=shuffle, n_pad=n_pad)
+    kp, vp, bad = orc.append(_bits(c.k_pool), _bits(c.v_pool), c.page_table.numpy(),
+                             _bits(c.k_new), _bits(c.v_new), c.batch_idx.numpy(),
+                             c.input_pos.numpy(), c.page_size)
+    assert bad == []
+    return c, kp, vp
+
+
+def check_paged_prefill_against_library(orc):
+    """One sequence with a 37-token prefix and a 29-token chunk: the chunk's
+    queries against the library's attention over the whole dense sequence,
+    masked by position."""
+    c, kp, vp = _chunk_case(orc, [37], [29], 16, 73, shuffle=False)
+    out, lse, bad = orc.paged_prefill_attention(_bits(c.q), kp, vp, c.page_table.numpy(),
+                                                c.batch_idx.numpy(), c.input_pos.numpy(),
+                                                c.page_size, c.scale)
+    assert bad == []
+    n = 37 + 29
+    rows = [int(c.page_table[1, t // 16]) * 16 + t % 16 for t in range(n)]
+    K = torch.from_numpy(orc.bf16_bits_to_f64(kp[rows])).permute(1, 0, 2)     # [Hkv, n, D]
+    V = torch.from_numpy(orc.bf16_bits_to_f64(vp[rows])).permute(1, 0, 2)
+    Q = torch.from_numpy(orc.bf16_bits_to_f64(_bits(c.q))).permute(1, 0, 2)   # [Hq, 29, D]
+    pos = c.input_pos.numpy()
+    mask = torch.from_numpy(np.arange(n)[None, :] <= pos[:, None])
+    ref_o, ref_l = _sdpa_with_probe(Q, K, V, mask)
+    assert np.allclose(out, ref_o.permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+    assert np.allclose(lse, ref_l.permute(1, 0).numpy(), rtol=0, atol=1e-10)
+
+
+def check_paged_prefill_reduces_to_packed_prefill(orc):
+    """Empty prefixes, chunks appended to the pages: exactly the packed
+    document-causal prefill over the same tokens."""
+    c, kp, vp = _chunk_case(orc, [0, 0, 0], [20, 1, 45], 16, 79, shuffle=False)
+    out, lse, bad = orc.paged_prefill_attention(_bits(c.q), kp, vp, c.page_table.numpy(),
+                                                c.batch_idx.numpy(), c.input_pos.numpy(),
+                                                c.page_size, c.scale)
+    ref_o, ref_l = orc.prefill_attention(_bits(c.q), _bits(c.k_new), _bits(c.v_new),
+                                         c.batch_idx.numpy(), c.input_pos.numpy(), c.scale)
+    assert bad == []
+    assert np.allclose(out, ref_o, rtol=0, atol=1e-12)
+    assert np.allclose(lse, ref_l, rtol=0, atol=1e-12)
+
+
+def check_paged_prefill_chunking_invariance(orc):
+    """A 70-token sequence in one chunk, or as chunks of 30 then 40 (the
+    first appended before the second is attended): the same results."""
+    from paged_kv_gqa_pkv_gb300 import workloads as W
+    whole, kp, vp = _chunk_case(orc, [0], [70], 16, 83, shuffle=False)
+    o_all, l_all, _ = orc.paged_prefill_attention(_bits(whole.q), kp, vp,
+                                                  whole.page_table.numpy(),
+                                                  whole.batch_idx.numpy(),
+                                                  whole.input_pos.numpy(), 16, whole.scale)
+    # chunk 2 of 40 tokens over a 30-token prefix: the same pools (the
+    # prefix's K/V are the first chunk's), queries 30..69
+    sel = np.arange(30, 70)
+    o2, l2, bad = orc.paged_prefill_attention(_bits(whole.q)[sel], kp, vp,
+                                              whole.page_table.numpy(),
+                                              whole.batch_idx.numpy()[sel],
+                                              whole.input_pos.numpy()[sel], 16, whole.scale)
+    assert bad == []
+    assert np.array_equal(o2, o_all[sel]) and np.array_equal(l2, l_all[sel])
+
+
+def check_paged_prefill_one_token_is_decode(orc):
+    """A chunk of one token per sequence is a decode step."""
+    c, kp, vp = _chunk_case(orc, [5, 0, 40, 17], [1, 1, 1, 1], 16, 89)
+    out, lse, bad = orc.paged_prefill_attention(_bits(c.q), kp, vp, c.page_table.numpy(),
+                                                c.batch_idx.numpy(), c.input_pos.numpy(),
+                                                c.page_size, c.scale)
+    d_o, d_l, d_bad = orc.decode_attention(_bits(c.q), kp, vp, c.page_table.numpy(),
+                                           c.batch_idx.numpy(), c.input_pos.numpy() + 1,
+                                           c.page_size, c.scale)
+    assert bad == [] and d_bad == []
+    assert np.array_equal(out, d_o) and np.array_equal(lse, d_l)
+
+
+def check_paged_prefill_order_and_edges(orc):
+    """Shuffling the packed order permutes the results; padding tokens give
+    0 / -inf; an unreserved page inside a token's keys makes it a bad row."""
+    c, kp, vp = _chunk_case(orc, [10, 33, 0], [7, 12, 19], 16, 97, shuffle=True, n_pad=3)
+    args = (kp, vp, c.page_table.numpy())
+    out, lse, bad = orc.paged_prefill_attention(_bits(c.q), *args, c.batch_idx.numpy(),
+                                                c.input_pos.numpy(), 16, c.scale)
+    assert bad == []
+    perm = np.random.default_rng(7).permutation(c.n_tokens)
+    o_p, l_p, _ = orc.paged_prefill_attention(_bits(c.q)[perm], *args, c.batch_idx.numpy()[perm],
+                                              c.input_pos.numpy()[perm], 16, c.scale)
+    assert np.array_equal(o_p, out[perm]) and np.array_equal(l_p, lse[perm])
+    pad = c.batch_idx.numpy() == 0
+    assert pad.sum() == 3 and np.all(out[pad] == 0) and np.all(np.isneginf(lse[pad]))
+    table = c.page_table.numpy().copy()
+    table[2, 1] = -1                    # slot 2 positions 16..31: its prefix of 33
+    _, _, bad2 = orc.paged_prefill_attention(_bits(c.q), kp, vp, table, c.batch_idx.numpy(),
+                                             c.input_pos.numpy(), 16, c.scale)
+    assert sorted(bad2) == sorted(np.nonzero(c.batch_idx.numpy() == 2)[0].tolist())
+
+
+ALL_CHECKS += [check_paged_prefill_against_library, check_paged_prefill_reduces_to_packed_prefill,
+               check_paged_prefill_chunking_invariance, check_paged_prefill_one_token_is_decode,
+               check_paged_prefill_order_and_edges]

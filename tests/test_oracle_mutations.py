@@ -218,7 +218,38 @@ def _append_rope_norm_after(k_pool, v_pool, table, k_new, v_new, bidx, pos, ps, 
     return _real_append_rope(k_pool, v_pool, table, k2, v_new, bidx, pos, ps, one, zero)
 
 
+def _paged_prefill_variant(excl_own=False, slot_of=None, skip_first=False):
+    def fn(q, k_pool, v_pool, page_table, batch_idx, input_pos, page_size, scale, rows=None):
+        T, hq, d = q.shape
+        out = np.full((T, hq, d), np.nan)
+        lse = np.full((T, hq), np.nan)
+        bad = []
+        for i in (range(T) if rows is None else rows):
+            slot = int(batch_idx[i]) if slot_of is None else slot_of(batch_idx, i)
+            if slot == 0:
+                out[i], lse[i] = 0.0, -np.inf
+                continue
+            n = int(input_pos[i]) + (0 if excl_own else 1)
+            K = orc.gather_logical(k_pool, page_table, slot, n, page_size)
+            V = orc.gather_logical(v_pool, page_table, slot, n, page_size)
+            if K is None or V is None or n <= 0:
+                bad.append(i)
+                continue
+            if skip_first and n > 1:
+                K, V = K[1:], V[1:]
+            out[i], lse[i] = orc.attend(orc.bf16_bits_to_f64(q[i]), K, V, scale)
+        return out, lse, bad
+    return fn
+
+
 MUTANTS.update({
+    "paged_prefill_excludes_own_token": ("paged_prefill_attention",
+                                         _paged_prefill_variant(excl_own=True)),
+    "paged_prefill_first_tokens_slot": ("paged_prefill_attention",
+                                        _paged_prefill_variant(
+                                            slot_of=lambda b, i: int(b[0]) if int(b[i]) else 0)),
+    "paged_prefill_drops_first_key": ("paged_prefill_attention",
+                                      _paged_prefill_variant(skip_first=True)),
     "k_norm_sum_not_mean": ("k_norm", _k_norm_sum),
     "k_norm_drops_eps": ("k_norm", _k_norm_no_eps),
     "k_norm_weight_reversed": ("k_norm", _k_norm_weight_reversed),
