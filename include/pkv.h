@@ -16,6 +16,8 @@
  *   pkv_append            - write new tokens' K/V rows through the page table
  *   pkv_append_rope       - the same with k_norm and the rotary embedding
  *                           applied to K
+ *   pkv_prefill_paged_attention - chunked prefill / mixed prefill + decode
+ *                           tokens attending their slots' keys through pages
  *   pkv_decode_attention  - one query token per row, GQA, over the pages
  *   pkv_prefill_attention - packed document-causal attention over fresh k/v
  *
@@ -236,6 +238,38 @@ pkv_status pkv_decode_attention_static_scratch(
     const int32_t* page_table, const void* q, int num_q_heads,
     const int32_t* batch_idx, const int32_t* seq_lens, int batch, float scale,
     void* out, float* lse, int32_t* dev_err, cudaStream_t stream);
+
+/*
+ * pkv_prefill_paged_attention - chunked prefill over the paged cache, on
+ * tcgen05 tensor cores. Source: the step the pages leave on the table
+ * ("flex_vs_vllm.md", "What's left on the table": chunked prefill, prefill
+ * and decode interleaved in one pass, reading earlier context from the
+ * pages); the per-token rule is the decode rule ("qwen3_flex_inference.py",
+ * _decode_block_mask, causal_offset: keys kv_idx <= input_pos).
+ *
+ * q: bf16 [n_tokens, num_q_heads, D], 16-byte aligned; batch_idx, input_pos:
+ * int32 [n_tokens]. Token i attends the logical keys 0..input_pos[i] of slot
+ * batch_idx[i], read through page_table from k_pool/v_pool:
+ *   lse[i, h] = ln sum_{t<=p} exp(scale * q[i,h] . K[slot,t,kvh])       (fp32)
+ *   out[i, h] = sum_{t<=p} exp(scale * q[i,h] . K[slot,t,kvh] - lse) V[slot,t,kvh]
+ * with kvh = h / (num_q_heads / num_kv_heads). The keys of the token's own
+ * chunk must be in the pools already (pkv_append first). Tokens need no order
+ * or packing: a chunk of a prompt is its tokens with consecutive positions, a
+ * decode token is a chunk of one, and both can share a call. Tokens of slot 0
+ * give out 0, lse -inf. A slot outside [0, max_batch) or a position outside
+ * [0, max_blocks * page_size) sets PKV_DEV_ERR_BAD_SLOT / _BAD_POS and gives
+ * 0 / -inf; an unreserved page entry among a token's keys sets
+ * PKV_DEV_ERR_BAD_PAGE and leaves that token's result unspecified.
+ * page_size must be 16, 32, 64 or a multiple of 128 (PKV_ERR_ARG otherwise);
+ * scale must be finite and > 0. The pools are only read.
+ */
+pkv_status pkv_prefill_paged_attention(const pkv_cache_desc* cache, const void* k_pool,
+                                       const void* v_pool, const int32_t* page_table,
+                                       const void* q, int num_q_heads,
+                                       const int32_t* batch_idx,
+                                       const int32_t* input_pos, int n_tokens,
+                                       float scale, void* out, float* lse,
+                                       int32_t* dev_err, cudaStream_t stream);
 
 /*
  * pkv_prefill_attention - packed document-causal prefill on tcgen05 tensor

@@ -32,7 +32,7 @@ DEV_ERR_LAYOUT = 0x8
 DEV_ERR_TIMEOUT = 0x10
 
 EXPORTED = ("pkv_append", "pkv_append_rope", "pkv_decode_workspace_size", "pkv_decode_attention",
-            "pkv_decode_append_attention",
+            "pkv_decode_append_attention", "pkv_prefill_paged_attention",
             "pkv_prefill_attention", "pkv_status_string",
             "pkv_status_from_device_error", "pkv_last_cuda_error_string")
 
@@ -83,6 +83,9 @@ def load_library() -> ctypes.CDLL:
                                                 i32p, c_int, c_float, vp, f32p, vp, c_size, i32p,
                                                 vp]
     lib.pkv_decode_append_attention.restype = c_int
+    lib.pkv_prefill_paged_attention.argtypes = [desc_p, vp, vp, i32p, vp, c_int, i32p, i32p,
+                                                c_int, c_float, vp, f32p, i32p, vp]
+    lib.pkv_prefill_paged_attention.restype = c_int
     lib.pkv_prefill_attention.argtypes = [vp, vp, vp, c_int, c_int, c_int, i32p, i32p, c_int,
                                           c_float, vp, f32p, i32p, vp]
     lib.pkv_prefill_attention.restype = c_int
@@ -262,6 +265,33 @@ def pkv_decode_append_attention(k_pool, v_pool, page_table, q, k_new, v_new, bat
         _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_err),
         _stream(stream))
     _check("pkv_decode_append_attention", st)
+    return out, lse
+
+
+def pkv_prefill_paged_attention(k_pool, v_pool, page_table, q, batch_idx, input_pos,
+                                page_size: int, scale: float, out=None, lse=None, dev_err=None,
+                                stream=None):
+    """Chunked prefill over the paged cache: token i of q [T, Hq, D] attends
+    its slot's keys 0..input_pos[i] through the page table (its own chunk
+    appended first). Returns (out [T, Hq, D] bf16, lse [T, Hq] fp32)."""
+    _need(q, "q", torch.bfloat16, 3)
+    for name, t, dt, nd in (("k_pool", k_pool, torch.bfloat16, 3),
+                            ("v_pool", v_pool, torch.bfloat16, 3),
+                            ("page_table", page_table, torch.int32, 2),
+                            ("batch_idx", batch_idx, torch.int32, 1),
+                            ("input_pos", input_pos, torch.int32, 1)):
+        _need(t, name, dt, nd)
+    T, hq, d = q.shape
+    if out is None:
+        out = torch.empty((T, hq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, hq), dtype=torch.float32, device=q.device)
+    desc = cache_desc(k_pool, page_table, page_size)
+    st = load_library().pkv_prefill_paged_attention(
+        ctypes.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(q), hq,
+        _ptr(batch_idx), _ptr(input_pos), T, float(scale), _ptr(out), _ptr(lse), _ptr(dev_err),
+        _stream(stream))
+    _check("pkv_prefill_paged_attention", st)
     return out, lse
 
 

@@ -329,6 +329,18 @@ pkv_status pkv_decode_append_attention(const pkv_cache_desc* cache, void* k_pool
                       dev_err, stream);
 }
 
+pkv_status pkv_prefill_paged_attention(const pkv_cache_desc* cache, const void* k_pool,
+                                      const void* v_pool, const int32_t* page_table,
+                                      const void* q, int num_q_heads, const int32_t* batch_idx,
+                                      const int32_t* input_pos, int n_tokens, float scale,
+                                      void* out, float* lse, int32_t* dev_err,
+                                      cudaStream_t stream) {
+  const pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  return pkv::prefill_paged_entry(cache, k_pool, v_pool, page_table, q, num_q_heads, batch_idx,
+                                  input_pos, n_tokens, scale, out, lse, dev_err, stream);
+}
+
 pkv_status pkv_prefill_attention(const void* q, const void* k, const void* v, int num_q_heads,
                                  int num_kv_heads, int head_dim, const int32_t* batch_idx,
                                  const int32_t* input_pos, int n_tokens, float scale, void* out,

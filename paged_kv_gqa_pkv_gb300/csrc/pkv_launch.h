@@ -97,6 +97,12 @@ pkv_status prefill_entry(const void* q, const void* k, const void* v, int num_q_
                          int num_kv_heads, int head_dim, const int32_t* batch_idx,
                          const int32_t* input_pos, int n_tokens, float scale, void* out,
                          float* lse, int32_t* dev_err, cudaStream_t stream);
+
+pkv_status prefill_paged_entry(const pkv_cache_desc* cache, const void* k_pool,
+                               const void* v_pool, const int32_t* page_table, const void* q,
+                               int num_q_heads, const int32_t* batch_idx,
+                               const int32_t* input_pos, int n_tokens, float scale, void* out,
+                               float* lse, int32_t* dev_err, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           int sm_count, cudaStream_t stream);
 

@@ -143,3 +143,17 @@ def test_decode_append_rejects_bad_arguments(lib):
     assert lib.pkv_decode_append_attention(*args(kn=264)) == 2
     assert lib.pkv_decode_append_attention(*args(hq=6)) == 1
     assert lib.pkv_decode_append_attention(*args(batch=0, kn=0, vn=0)) == 0
+
+
+def test_prefill_paged_rejects_bad_arguments(lib):
+    args = lambda ps=16, hq=8, n=16, q=256, scale=0.088: (  # noqa: E731
+        ctypes.byref(_desc(page_size=ps)), P(256), P(256), P(256), P(q), hq, P(256), P(256), n,
+        ctypes.c_float(scale), P(256), P(256), None, None)
+    assert lib.pkv_prefill_paged_attention(*args(ps=48)) == 1      # tiles would straddle pages
+    assert lib.pkv_prefill_paged_attention(*args(ps=24)) == 1      # not a multiple of 16
+    assert lib.pkv_prefill_paged_attention(*args(hq=6)) == 1
+    assert lib.pkv_prefill_paged_attention(*args(n=-1)) == 1
+    assert lib.pkv_prefill_paged_attention(*args(scale=0.0)) == 1
+    assert lib.pkv_prefill_paged_attention(*args(q=264)) == 2
+    assert lib.pkv_prefill_paged_attention(*args(n=0)) == 0
+    assert lib.pkv_prefill_paged_attention(*args(ps=256, n=0)) == 0
