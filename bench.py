@@ -450,6 +450,43 @@ def run_pkv(args):
                 "append_gbs": (c.n_tokens * c.num_kv_heads * c.head_dim * 2 * 4)
                 / (app_us * 1e-6) / 1e9}
 
+    def timed_chunked_prefill(reps, n_decode=0):
+        """Chunked prefill over the paged cache: 16 chunks of 512 tokens over
+        prefixes U[512, 4096] (T=8192), pages permuted, plus `n_decode` decode
+        tokens for a mixed step. The chunk K/V are appended once; the tcgen05
+        paged attention is timed with CUDA events over `reps` back-to-back
+        calls (the pools, ~450 MB, exceed L2)."""
+        c = W.chunked_prefill(0, n_decode=n_decode)
+        q, bi, ip = c.q.to(dev), c.batch_idx.to(dev), c.input_pos.to(dev)
+        kp, vp, pt = c.k_pool.to(dev), c.v_pool.to(dev), c.page_table.to(dev)
+        out = torch.empty_like(q)
+        lse = torch.empty((c.n_tokens, c.num_q_heads), dtype=torch.float32, device=dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        binding.pkv_append(kp, vp, pt, c.k_new.to(dev), c.v_new.to(dev), bi, ip, c.page_size,
+                           dev_err=err)
+        for _ in range(3):
+            binding.pkv_prefill_paged_attention(kp, vp, pt, q, bi, ip, c.page_size, c.scale,
+                                                out=out, lse=lse, dev_err=err)
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record()
+        for _ in range(reps):
+            binding.pkv_prefill_paged_attention(kp, vp, pt, q, bi, ip, c.page_size, c.scale,
+                                                out=out, lse=lse, dev_err=err)
+        ev[1].record()
+        torch.cuda.synchronize()
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(err.item()):#x} in chunked prefill")
+        att_us = ev[0].elapsed_time(ev[1]) / reps * 1e3
+        flops = 4.0 * c.head_dim * c.num_q_heads * c.info["pairs"]
+        tf = flops / (att_us * 1e-6) / 1e12
+        return {"workload": f"chunked_prefill: 16 chunks of 512 over prefixes U[512,4096] + "
+                            f"{n_decode} decode tokens, T={c.n_tokens}, Hq=32, Hkv=8, D=128, "
+                            f"page 128, permuted pages, seed 0",
+                "attention_call_us": att_us, "algorithmic_flops": flops, "tflops": tf,
+                "bound": "tensor", "peak_tflops": bf16_peak, "frac": tf / bf16_peak,
+                "peak_kind": peak_kind}
+
     from paged_kv_gqa_pkv_gb300 import sharding
     # each rank serves its own shard of independent sequences (weak scaling)
     case = W.qwen3_b64_decode(sharding.shard_seed(rank), permute=False)
@@ -471,6 +508,11 @@ def run_pkv(args):
     rp = timed_decode(perm, max(args.steps // 4, 10), args.warmup)
     e2e_ms, h2d, d2h = e2e_decode(case, max(args.steps // 10, 10), args.warmup)
     prefill = timed_prefill(20)
+    chunked = timed_chunked_prefill(20)
+    mixed = timed_chunked_prefill(20, n_decode=48)
+    chunked["mixed_step_with_48_decode_tokens"] = {
+        "attention_call_us": mixed["attention_call_us"], "tflops": mixed["tflops"],
+        "frac": mixed["frac"]}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -500,6 +542,7 @@ def run_pkv(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
         "prefill": prefill,
+        "chunked_prefill": chunked,
         "gpu_launches": 2 * args.steps,
         "clocks": r["clocks"],
     }
