@@ -49,7 +49,7 @@ constexpr int kKTileBytes = kDecodeTile * kHeadDim * 2;  // one head, 16 tokens 
 
 template <int G>
 struct DecodeCfg {
-  static constexpr int kStages = (G >= 8) ? 2 : kDecodeStages;
+  static constexpr int kStages = kDecodeStages;
   static constexpr int kQBytes = G * kHeadDim * 2;
   // stage: K tile (two 2 KB swizzled halves), V tile (same), q rows
   static constexpr int kOffV = kKTileBytes;
