@@ -485,7 +485,8 @@ def run_pkv(args):
                             f"page 128, permuted pages, seed 0",
                 "attention_call_us": att_us, "algorithmic_flops": flops, "tflops": tf,
                 "bound": "tensor", "peak_tflops": bf16_peak, "frac": tf / bf16_peak,
-                "peak_kind": peak_kind}
+                "peak_kind": peak_kind,
+                "traffic": captured_traffic("chunked_prefill_call") if n_decode == 0 else None}
 
     from paged_kv_gqa_pkv_gb300 import sharding
     # each rank serves its own shard of independent sequences (weak scaling)
