@@ -369,31 +369,50 @@ def run_pkv(args):
 
     def e2e_decode(case, steps, warmup):
         """Same step through the public binding with pinned host buffers: each
-        step copies its inputs host->device and reads the result back."""
+        step copies its inputs host->device and reads the result back. The
+        inputs are staged the way a serving loop would: q, the new K/V,
+        batch_idx, seq_lens and the page table in one pinned host buffer and
+        one device buffer (each tensor a 256-byte aligned view), out and lse
+        in one output buffer, so a step is one H2D copy, the fused call and
+        one D2H copy, then a stream sync."""
         s = make_sets(case, 1)[0]
-        host = {k: getattr(case, a).pin_memory() for k, a in
-                (("q", "q"), ("kn", "k_new"), ("vn", "v_new"), ("bi", "batch_idx"),
-                 ("sl", "seq_lens"), ("pt", "page_table"))}
         B, hq = case.batch, case.num_q_heads
-        out_h = torch.empty((B, hq, 128), dtype=torch.bfloat16).pin_memory()
-        lse_h = torch.empty((B, hq), dtype=torch.float32).pin_memory()
-        ws = torch.empty(binding.pkv_decode_workspace_size(s["kp"], s["pt"], case.page_size,
+
+        def staged(parts, device, pin=False):
+            offs, n = {}, 0
+            for k, t in parts:
+                offs[k] = n
+                n += (t.numel() * t.element_size() + 255) // 256 * 256
+            buf = torch.zeros(n, dtype=torch.uint8, device=device)
+            if pin:
+                buf = buf.pin_memory()
+            views = {k: buf[offs[k]:offs[k] + t.numel() * t.element_size()].view(t.dtype)
+                     .view(t.shape) for k, t in parts}
+            return buf, views
+
+        ins = [("q", case.q), ("kn", case.k_new), ("vn", case.v_new),
+               ("bi", case.batch_idx), ("sl", case.seq_lens), ("pt", case.page_table)]
+        host_in, hv = staged(ins, "cpu", pin=True)
+        for k, t in ins:
+            hv[k].copy_(t)
+        dev_in, dv = staged(ins, dev)
+        outs = [("out", torch.empty((B, hq, 128), dtype=torch.bfloat16)),
+                ("lse", torch.empty((B, hq), dtype=torch.float32))]
+        dev_out, ov = staged(outs, dev)
+        host_out = torch.empty(dev_out.numel(), dtype=torch.uint8).pin_memory()
+        ws = torch.empty(binding.pkv_decode_workspace_size(s["kp"], dv["pt"], case.page_size,
                                                            B, hq),
                          dtype=torch.uint8, device=dev)
-        out = torch.empty((B, hq, 128), dtype=torch.bfloat16, device=dev)
-        lse = torch.empty((B, hq), dtype=torch.float32, device=dev)
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
-        d2h = out_h.numel() * 2 + lse_h.numel() * 4
+        h2d = host_in.numel()
+        d2h = host_out.numel()
 
         def step():
-            for k, t in host.items():
-                s[k].copy_(t, non_blocking=True)
-            binding.pkv_decode_append_attention(s["kp"], s["vp"], s["pt"], s["q"], s["kn"],
-                                                s["vn"], s["bi"], s["sl"], case.page_size,
-                                                case.scale, out=out, lse=lse, workspace=ws,
-                                                stream=stream)
-            out_h.copy_(out, non_blocking=True)
-            lse_h.copy_(lse, non_blocking=True)
+            dev_in.copy_(host_in, non_blocking=True)
+            binding.pkv_decode_append_attention(s["kp"], s["vp"], dv["pt"], dv["q"], dv["kn"],
+                                                dv["vn"], dv["bi"], dv["sl"], case.page_size,
+                                                case.scale, out=ov["out"], lse=ov["lse"],
+                                                workspace=ws, stream=stream)
+            host_out.copy_(dev_out, non_blocking=True)
             stream.synchronize()
 
         for _ in range(warmup):
