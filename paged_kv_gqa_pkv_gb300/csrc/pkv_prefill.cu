@@ -405,8 +405,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
         if (!none) {
           float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
           if (full) {
-#pragma unroll
-            for (int c = 0; c < kBN; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sr[c]));
+            m4[0] = row_max_full(sr);
           } else {
             const unsigned span = static_cast<unsigned>(c_hi - c_lo);
 #pragma unroll
@@ -449,19 +448,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
             *reinterpret_cast<uint4*>(sP + (q >> 3) * kHalf + row * 128 +
                                       (((q & 7) ^ (row & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
         } else {
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            float e[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u)  // ex2(-inf) = +0 for masked keys
-              e[u] = ex2(fmaf(__uint_as_float(sr[8 * q + u]), p.qscale, neg_m));
-            psum += ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
-            // 16-byte chunk q of this row (K-major SW128): half q>>3, position (q&7)^(row&7)
-            *reinterpret_cast<uint4*>(sP + (q >> 3) * kHalf + row * 128 +
-                                      (((q & 7) ^ (row & 7)) << 4)) =
-                make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
-                           pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
-          }
+          psum = softmax_row_to_p(sr, p.qscale, neg_m, sP, row);
         }
         l_run = l_run * alpha + psum;
         m_run = m_use;

@@ -39,6 +39,82 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Two fp32 lanes per instruction (Blackwell's paired FMA/ADD).
+__device__ __forceinline__ unsigned long long pack_f32x2(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack_f32x2(unsigned long long v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b,
+                                                    unsigned long long c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ unsigned long long fadd2(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// Maximum of a fully visible 128-column S row (three-input max, four chains).
+__device__ __forceinline__ float row_max_full(const uint32_t (&sr)[128]) {
+  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int c = 0; c < 128; c += 8) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      m[k] = fmax3(m[k], __uint_as_float(sr[c + 2 * k]), __uint_as_float(sr[c + 2 * k + 1]));
+  }
+  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
+// One softmax row of a 128-key tile: P = exp2(s * qscale - m) written as bf16
+// into this row of the K-major 128-byte-swizzled P tile (16-byte chunk q at
+// half q >> 3, position (q & 7) ^ (row & 7)); returns the row's sum of P in
+// fp32. Masked columns hold -inf, which ex2.approx maps to +0 exactly. The
+// scale-and-shift and the sum run two lanes per instruction: the softmax is
+// bound by instruction issue, not by the exponential unit (moving a quarter
+// of the exponentials to an FMA-pipe polynomial made the kernel 8 % slower).
+__device__ __forceinline__ float softmax_row_to_p(const uint32_t (&sr)[128], float qscale,
+                                                  float neg_m, uint8_t* sP, int row) {
+  const unsigned long long qs2 = pack_f32x2(qscale, qscale);
+  const unsigned long long nm2 = pack_f32x2(neg_m, neg_m);
+  unsigned long long acc0 = 0ull, acc1 = 0ull;  // two paired partial sums (0.0f, 0.0f)
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    float e[8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const unsigned long long x2 = ffma2(
+          pack_f32x2(__uint_as_float(sr[8 * q + 2 * u]), __uint_as_float(sr[8 * q + 2 * u + 1])),
+          qs2, nm2);
+      float x0, x1;
+      unpack_f32x2(x2, x0, x1);
+      e[2 * u] = ex2(x0);
+      e[2 * u + 1] = ex2(x1);
+    }
+    acc0 = fadd2(acc0, fadd2(pack_f32x2(e[0], e[1]), pack_f32x2(e[2], e[3])));
+    acc1 = fadd2(acc1, fadd2(pack_f32x2(e[4], e[5]), pack_f32x2(e[6], e[7])));
+    *reinterpret_cast<uint4*>(sP + (q >> 3) * kHalf + row * 128 + (((q & 7) ^ (row & 7)) << 4)) =
+        make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]), pack_bf16x2(e[4], e[5]),
+                   pack_bf16x2(e[6], e[7]));
+  }
+  float a, b, c, d;
+  unpack_f32x2(acc0, a, b);
+  unpack_f32x2(acc1, c, d);
+  return (a + b) + (c + d);
+}
+
 // Bounded wait that also gives up when another role has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
                                               volatile int* abort_flag) {

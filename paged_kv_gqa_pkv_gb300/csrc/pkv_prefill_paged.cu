@@ -527,8 +527,7 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
         if (!none) {
           float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
           if (full) {
-#pragma unroll
-            for (int q = 0; q < kBN; ++q) m4[q & 3] = fmaxf(m4[q & 3], __uint_as_float(sr[q]));
+            m4[0] = row_max_full(sr);
           } else {
 #pragma unroll
             for (int q = 0; q < kBN; ++q) {
@@ -566,18 +565,7 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
             *reinterpret_cast<uint4*>(sP + (q >> 3) * kHalf + row * 128 +
                                       (((q & 7) ^ (row & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
         } else {
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            float e[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u)  // ex2(-inf) = +0 for masked keys
-              e[u] = ex2(fmaf(__uint_as_float(sr[8 * q + u]), p.qscale, neg_m));
-            psum += ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
-            *reinterpret_cast<uint4*>(sP + (q >> 3) * kHalf + row * 128 +
-                                      (((q & 7) ^ (row & 7)) << 4)) =
-                make_uint4(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]),
-                           pack_bf16x2(e[4], e[5]), pack_bf16x2(e[6], e[7]));
-          }
+          psum = softmax_row_to_p(sr, p.qscale, neg_m, sP, row);
         }
         l_run = l_run * alpha + psum;
         m_run = m_use;
