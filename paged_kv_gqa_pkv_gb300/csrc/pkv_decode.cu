@@ -188,9 +188,91 @@ __device__ __forceinline__ void load_row_pages(RowPages& rp, const DecodeParams&
   rp.contiguous = ok;
 }
 
+// An item split over more than this many warps ("long": few rows, many
+// keys) has the partials of each CTA combined inside the CTA, so the merge
+// kernel sees one segment per CTA instead of one per warp.
+constexpr int kLongItemSegs = 24;
+
+// Combines the k <= 8 partials that consecutive warps wa .. wa+k-1 of one CTA
+// left for item (b, kvh) (slots wa + item ...), all G heads at once, by LSE in
+// log2 units: lanes take segments for (m, l) and four head dims each for o.
+// With final_out the item is complete (it lies inside the CTA): out and lse
+// are written; otherwise the merged partial replaces the first slot's.
+template <int G>
+__device__ __forceinline__ void combine_segments(const DecodeParams& p, int b, int kvh, int wa,
+                                                 int k, bool final_out, int lane) {
+  constexpr int SF = decode_slot_floats(G);
+  const int hkv = p.num_kv_heads;
+  float* base = p.partials + (static_cast<int64_t>(wa) + static_cast<int64_t>(b) * hkv + kvh) * SF;
+  float M[G], L[G], sc[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float m = -INFINITY, l = 0.f;
+    if (lane < k) {
+      m = __ldcg(base + static_cast<int64_t>(lane) * SF + G * kHeadDim + h);
+      l = __ldcg(base + static_cast<int64_t>(lane) * SF + G * kHeadDim + G + h);
+    }
+    float mx = m;
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    mx = __shfl_sync(0xffffffffu, mx, 0);
+    sc[h] = lane < k ? exp2f(m - mx) : 0.f;
+    float ls = l * sc[h];
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+    M[h] = mx;
+    L[h] = __shfl_sync(0xffffffffu, ls, 0);
+  }
+  float4 acc[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < kDecodeWarps; ++j) {
+    if (j < k) {
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float s = __shfl_sync(0xffffffffu, sc[h], j);
+        const float4 ov = __ldcg(reinterpret_cast<const float4*>(
+            base + static_cast<int64_t>(j) * SF + h * kHeadDim + lane * 4));
+        acc[h].x = fmaf(ov.x, s, acc[h].x);
+        acc[h].y = fmaf(ov.y, s, acc[h].y);
+        acc[h].z = fmaf(ov.z, s, acc[h].z);
+        acc[h].w = fmaf(ov.w, s, acc[h].w);
+      }
+    }
+  }
+  if (final_out) {
+    const int64_t head0 = static_cast<int64_t>(b) * p.num_q_heads + kvh * G;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float inv = 1.f / L[h];
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[h].x * inv, acc[h].y * inv);
+      const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[h].z * inv, acc[h].w * inv);
+      uint2 packed;
+      packed.x = *reinterpret_cast<const uint32_t*>(&lo);
+      packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + (head0 + h) * kHeadDim +
+                                lane * 4) = packed;
+      if (lane == h) p.lse[head0 + h] = (M[h] + log2f(L[h])) * 0.69314718055994531f;
+    }
+  } else {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      *reinterpret_cast<float4*>(base + h * kHeadDim + lane * 4) = acc[h];
+      if (lane == h) {
+        base[G * kHeadDim + h] = M[h];
+        base[G * kHeadDim + G + h] = L[h];
+      }
+    }
+  }
+}
+
 }  // namespace
 
-template <int G>
+// kCombine: the launch expects long items (few rows for the machine) and the
+// CTAs combine their partials of those; without it the code below it is
+// compiled out and every item goes to the merge kernel one segment per warp.
+template <int G, bool kCombine>
 __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
@@ -266,7 +348,10 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
   const int64_t per = (total + p.num_workers - 1) / p.num_workers;
   const int64_t u_begin = static_cast<int64_t>(worker) * per;
   const int64_t u_end = min(u_begin + per, total);
-  if (u_begin >= u_end) return;
+  if constexpr (!kCombine) {
+    if (u_begin >= u_end) return;
+  }
+  if (u_begin < u_end) {
   const int count = static_cast<int>(u_end - u_begin);
 
   const Cursor start = locate(s_prefix, B, hkv, u_begin);
@@ -533,14 +618,72 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
       mbar_wait_bounded(&bars[s], (k / S) & 1);
     }
   }
+  }  // this warp's range
+
+  // ---- long items (split over more than kLongItemSegs warps) that two or
+  // more warps of this CTA share are combined here into one partial, in the
+  // slot of this CTA's first warp on the item. A long item always crosses
+  // CTAs, so the merge kernel finishes it from one segment per CTA. Every
+  // warp walks the CTA's items alike, so the barrier is taken CTA-uniformly
+  // and only by CTAs that hold such an item.
+  if constexpr (kCombine) {
+    const int64_t span = static_cast<int64_t>(kDecodeWarps) * per;
+    const int64_t U0 = static_cast<int64_t>(blockIdx.x) * span;
+    const int64_t U1 = min(U0 + span, total);
+    const int wlo = blockIdx.x * kDecodeWarps;
+    const int whi = wlo + kDecodeWarps - 1;
+    // visits the items overlapping this CTA's tiles; f(cursor, w0, w1, wa, wb)
+    auto for_items = [&](auto&& f) {
+      if (U0 >= U1) return;
+      Cursor c = locate(s_prefix, B, hkv, U0);
+      int64_t u_s = U0 - c.tile;  // the item's first tile
+      while (true) {
+        const int64_t u_e = u_s + c.tiles - 1;
+        const int w0 = static_cast<int>(u_s / per);
+        const int w1 = static_cast<int>(u_e / per);
+        f(c, w0, w1, max(w0, wlo), min(w1, whi));
+        if (u_e + 1 >= U1) break;
+        c.tile = c.tiles - 1;
+        advance(c, s_prefix, hkv);
+        u_s = u_e + 1;
+      }
+    };
+    // An item of t tiles spans at most (t - 1) / per + 2 warps: with no row
+    // longer than (kLongItemSegs - 2) * per tiles there is nothing to combine
+    // and the walk below is skipped (the common case).
+    int longest = 0;
+    for (int r = lane; r < B; r += 32) longest = max(longest, s_prefix[r + 1] - s_prefix[r]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) longest = max(longest, __shfl_xor_sync(0xffffffffu, longest, o));
+    bool any = false;
+    if (static_cast<int64_t>(longest) > static_cast<int64_t>(kLongItemSegs - 2) * per) {
+      for_items([&](const Cursor&, int w0, int w1, int wa, int wb) {
+        if (w1 - w0 + 1 > kLongItemSegs && wb > wa) any = true;
+      });
+    }
+    if (any) {
+      __syncthreads();    // every warp's partials are written
+      pdl_wait_primary();  // idle warps skipped the wait above
+      int q = 0;
+      for_items([&](const Cursor& c, int w0, int w1, int wa, int wb) {
+        if (w1 - w0 + 1 > kLongItemSegs && wb > wa) {
+          if (q % kDecodeWarps == warp)
+            combine_segments<G>(p, c.b, c.kvh, wa, wb - wa + 1, /*final_out=*/false, lane);
+          ++q;
+        }
+      });
+    }
+  }
 }
 
 // One warp per (row, q head). The warp rebuilds the split-KV schedule from
 // the call's inputs (row tile counts and their prefix) before waiting on the
 // split-KV grid, so after the wait only the partials are read: for items of
-// up to 8 segments, (m, l) and all o rows go out in one round of loads.
-template <int G>
+// up to kFast segments (16 with kByCta, else 8), (m, l) and all o rows go out
+// in one round of loads.
+template <int G, bool kByCta>
 __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p) {
+  constexpr int kFast = kByCta ? 16 : 8;
   // The next launch may start its prologue now; it touches the workspace
   // only after this grid completes.
   pdl_launch_dependents();
@@ -579,33 +722,42 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
   const int64_t per = (static_cast<int64_t>(total) * hkv + p.num_workers - 1) / p.num_workers;
   const int64_t u0 = static_cast<int64_t>(before) * hkv + static_cast<int64_t>(kvh) * tiles;
   const int w0 = static_cast<int>(u0 / per);
-  const int nseg = static_cast<int>((u0 + tiles - 1) / per) - w0 + 1;
-  if (nseg == 1) return;  // written by the split-KV pass
+  const int w1 = static_cast<int>((u0 + tiles - 1) / per);
+  if (w0 == w1) return;  // one warp: written by the split-KV pass
+  // a long item was combined per CTA by the split-KV pass: one segment per
+  // CTA, in the slot of that CTA's first warp on it; else one per warp
+  const bool by_cta = kByCta && w1 - w0 + 1 > kLongItemSegs;
+  const int c0 = w0 / kDecodeWarps;
+  const int nseg = by_cta ? w1 / kDecodeWarps - c0 + 1 : w1 - w0 + 1;
   constexpr int SF = decode_slot_floats(G);
-  const float* slots = p.partials + (static_cast<int64_t>(w0) + static_cast<int64_t>(b) * hkv + kvh) * SF;
+  const float* item_slots = p.partials + (static_cast<int64_t>(b) * hkv + kvh) * SF;
+  auto seg = [&](int s) -> const float* {
+    const int w = by_cta ? (s == 0 ? w0 : (c0 + s) * kDecodeWarps) : w0 + s;
+    return item_slots + static_cast<int64_t>(w) * SF;
+  };
 
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float M, L = 0.f;
-  if (nseg <= 8) {
+  if (nseg <= kFast) {
     float ms = -INFINITY, ls = 0.f;
     if (lane < nseg) {
-      ms = __ldcg(slots + static_cast<int64_t>(lane) * SF + G * kHeadDim + g);
-      ls = __ldcg(slots + static_cast<int64_t>(lane) * SF + G * kHeadDim + G + g);
+      ms = __ldcg(seg(lane) + G * kHeadDim + g);
+      ls = __ldcg(seg(lane) + G * kHeadDim + G + g);
     }
-    float4 ov[8];
+    float4 ov[kFast];
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+    for (int j = 0; j < kFast; ++j)
       if (j < nseg)
-        ov[j] = __ldcg(reinterpret_cast<const float4*>(slots + static_cast<int64_t>(j) * SF +
+        ov[j] = __ldcg(reinterpret_cast<const float4*>(seg(j) +
                                                        g * kHeadDim + lane * 4));
     M = ms;
 #pragma unroll
-    for (int o = 4; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    for (int o = kFast / 2; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     M = __shfl_sync(0xffffffffu, M, 0);
     const float sc = (lane < nseg) ? exp2f(ms - M) : 0.f;
     L = ls * sc;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < kFast; ++j) {
       const float scj = __shfl_sync(0xffffffffu, sc, j);
       if (j < nseg) {
         acc.x = fmaf(ov[j].x, scj, acc.x);
@@ -618,7 +770,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
     M = -INFINITY;
     for (int s0 = 0; s0 < nseg; s0 += 32) {
       const int s = s0 + lane;
-      if (s < nseg) M = fmaxf(M, __ldcg(slots + static_cast<int64_t>(s) * SF + G * kHeadDim + g));
+      if (s < nseg) M = fmaxf(M, __ldcg(seg(s) + G * kHeadDim + g));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -626,7 +778,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
       const int s = s0 + lane;
       float sc = 0.f;
       if (s < nseg) {
-        const float* sl = slots + static_cast<int64_t>(s) * SF;
+        const float* sl = seg(s);
         sc = exp2f(__ldcg(sl + G * kHeadDim + g) - M);
         L = fmaf(__ldcg(sl + G * kHeadDim + G + g), sc, L);
       }
@@ -635,7 +787,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
       for (int j = 0; j < n; ++j) {
         const float scj = __shfl_sync(0xffffffffu, sc, j);
         const float4 ov = __ldcg(reinterpret_cast<const float4*>(
-            slots + static_cast<int64_t>(s0 + j) * SF + g * kHeadDim + lane * 4));
+            seg(s0 + j) + g * kHeadDim + lane * 4));
         acc.x = fmaf(ov.x, scj, acc.x);
         acc.y = fmaf(ov.y, scj, acc.y);
         acc.z = fmaf(ov.z, scj, acc.z);
@@ -663,9 +815,9 @@ size_t decode_workspace_bytes(int batch, int num_kv_heads, int group, int num_wo
 
 int decode_workers_for_device(int sm_count) { return sm_count * kDecodeWarps; }
 
-template <int G>
-static cudaError_t launch_decode_g(const DecodeParams& p, const CUtensorMap& kmap,
-                                   const CUtensorMap& vmap, int sm_count, cudaStream_t stream) {
+template <int G, bool kCombine>
+static cudaError_t launch_decode_gc(const DecodeParams& p, const CUtensorMap& kmap,
+                                    const CUtensorMap& vmap, int sm_count, cudaStream_t stream) {
   using C = DecodeCfg<G>;
   const size_t smem = C::smem_bytes(p.batch);
   static_assert(C::smem_bytes(kDecodeMaxBatch) <= 232448, "decode shared memory over budget");
@@ -677,17 +829,29 @@ static cudaError_t launch_decode_g(const DecodeParams& p, const CUtensorMap& kma
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(decode_splitkv_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(decode_splitkv_kernel<G, kCombine>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::smem_bytes(kDecodeMaxBatch)));
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  e = launch_kernel(decode_splitkv_kernel<G>, dim3(sm_count), dim3(kDecodeWarps * 32), smem,
-                    stream, /*programmatic=*/true, kmap, vmap, p);
+  e = launch_kernel(decode_splitkv_kernel<G, kCombine>, dim3(sm_count), dim3(kDecodeWarps * 32),
+                    smem, stream, /*programmatic=*/true, kmap, vmap, p);
   if (e != cudaSuccess) return e;
   const int rows = p.batch * p.num_q_heads;
-  return launch_kernel(decode_merge_kernel<G>, dim3((rows + 7) / 8), dim3(256), 0, stream,
-                       /*programmatic=*/true, p);
+  return launch_kernel(decode_merge_kernel<G, kCombine>, dim3((rows + 7) / 8), dim3(256), 0,
+                       stream, /*programmatic=*/true, p);
+}
+
+// Few (row, kv head) items for the machine's workers means long items: then
+// the CTAs combine their partials of those before the merge.
+template <int G>
+static cudaError_t launch_decode_g(const DecodeParams& p, const CUtensorMap& kmap,
+                                   const CUtensorMap& vmap, int sm_count, cudaStream_t stream) {
+  const bool combine =
+      static_cast<int64_t>(p.batch) * p.num_kv_heads * kLongItemSegs < p.num_workers;
+  return combine ? launch_decode_gc<G, true>(p, kmap, vmap, sm_count, stream)
+                 : launch_decode_gc<G, false>(p, kmap, vmap, sm_count, stream);
 }
 
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,

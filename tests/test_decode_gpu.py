@@ -200,3 +200,15 @@ def test_short_rows_finish_whole_items_in_one_worker():
     c = W.custom_decode(23, lens, hq=32, hkv=8, page_size=16, permute=True)
     _full_parity(c)
 
+
+
+@pytest.mark.parametrize("lens,hq,hkv,ps", [([5000, 12, 7000], 32, 8, 128),
+                                            ([9000, 8191], 8, 2, 64),
+                                            ([20000], 32, 8, 16)],
+                         ids=["b3_h8", "b2_g4_h2", "b1_20k_ps16"])
+def test_long_rows_small_batch_combined_per_cta(lens, hq, hkv, ps):
+    """Few rows with many keys: items are split over dozens of warps, and the
+    CTAs combine their parts before the merge (the launch picks that path
+    for small batch x kv heads)."""
+    c = W.custom_decode(29, lens, hq=hq, hkv=hkv, page_size=ps, permute=True)
+    _full_parity(c)
