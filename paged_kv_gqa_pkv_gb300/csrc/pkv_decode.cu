@@ -15,12 +15,16 @@
 // 16-token tiles of every (row, kv head) item. Every CTA recomputes the
 // per-row tile prefix sum in shared memory; the list is cut into
 // num_workers = SMs x 8 equal contiguous ranges, one per warp. A warp streams
-// its range through a private ring of TMA stages (K tile, V tile and, at a
-// segment start, the item's G query rows), so no barrier is shared between
-// warps. Each (worker, item) segment leaves one partial (unnormalised o for
-// the G heads, running max m and sum l in log2 units) in slot
-// worker + item, unique because both indices grow along the list. The merge
-// kernel combines an item's segments by LSE.
+// its range through a private two-stage ring of TMA stages (K tile, V tile
+// and, at a segment start, the item's G query rows), so no barrier is shared
+// between warps. An item that lies inside one warp's range is normalised and
+// written by that warp. Every other (worker, item) segment leaves one partial
+// (unnormalised o for the G heads, running max m and sum l in log2 units) in
+// slot worker + item, unique because both indices grow along the list, and
+// the merge kernel combines an item's segments by LSE. When the launch
+// expects long items (few rows for the machine, kCombine), the CTAs first
+// combine their warps' partials of items split over more than kLongItemSegs
+// warps, so the merge reads one segment per CTA for those.
 //
 // Arithmetic per tile: all G query heads of a kv head use one load of each K
 // and V row. The two products are small dense contractions and run as
@@ -122,21 +126,6 @@ __device__ __forceinline__ void advance(Cursor& c, const int32_t* prefix, int hk
     ++c.b;
     c.tiles = prefix[c.b + 1] - prefix[c.b];
   } while (c.tiles == 0);
-}
-
-// One reduce-scatter step across lanes `lane ^ M`: of 2*H partial sums, a lane
-// keeps the lower H (bit M of the lane clear) or the upper H, adding its
-// partner's copy of them.
-template <int H, int M>
-__device__ __forceinline__ void rs_step(float* v, int lane, int& idx0) {
-  const bool upper = (lane & M) != 0;
-#pragma unroll
-  for (int i = 0; i < H; ++i) {
-    const float send = upper ? v[i] : v[i + H];
-    const float keep = upper ? v[i + H] : v[i];
-    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, M);
-  }
-  if (upper) idx0 += H;
 }
 
 // Fused append: the new token of item (b, kvh), at position seq_lens[b] - 1,
