@@ -44,6 +44,19 @@ namespace {
 
 using namespace prefill_detail;
 
+// shared memory layout (offsets from a 1024-aligned base)
+constexpr int kRing = 3;                              // K/V tile slots
+constexpr int kOffQ = 0;                              // Q0, Q1
+constexpr int kOffP = kOffQ + 2 * kTileBytes;         // P0, P1 (also output staging)
+constexpr int kOffRing = kOffP + 2 * kTileBytes;      // kRing slots
+constexpr int kOffBar = kOffRing + kRing * kTileBytes;
+// q_full, q_empty, ring_full[3], ring_empty[3], s_full[2], p_full[2],
+// pv_done[2], o_free[2], s_free[2], grp_sync[2]
+constexpr int kNumBars = 20;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;      // tmem slot, abort flag
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;      // + slack for 1024 alignment
+static_assert(kSmemBytes <= kMaxDynSmem, "shared memory above the opt-in limit");
+
 struct PrefillParams {
   const int32_t* batch_idx;
   const int32_t* input_pos;

@@ -1,7 +1,9 @@
 // pkv_prefill_common.cuh - what the two tcgen05 prefill kernels share: tile
-// sizes, the shared-memory layout, the MMA instruction descriptors, the
-// bounded wait that honours a grid-wide abort flag, and the host-side
-// cuTensorMapEncodeTiled lookup.
+// sizes, the tensor-memory layout, the MMA instruction descriptors, the
+// softmax row (P into shared memory for the packed kernel, into tensor memory
+// for the paged one), the bounded wait that honours a grid-wide abort flag,
+// and the host-side cuTensorMapEncodeTiled lookup. Each kernel file lays out
+// its own shared memory.
 #pragma once
 
 #include "pkv_launch.h"
@@ -13,25 +15,42 @@ constexpr int kBM = 128;                 // query rows per tile
 constexpr int kBN = 128;                 // keys per KV tile
 constexpr int kHalf = 128 * 128;         // one [128 rows x 64 elems] bf16 block, bytes
 constexpr int kTileBytes = 2 * kHalf;    // 128 x 128 bf16 (32 KB)
-constexpr int kRing = 3;                 // K/V half-stage slots
 constexpr int kThreads = 10 * 32;
 constexpr int kGroupThreads = 128;       // one softmax warpgroup
-constexpr uint32_t kTmemCols = 512;      // S0 S1 O0 O1, 128 columns each
+// TMEM columns: S0 S1 O0 O1, 128 each. Where P lives in TMEM, P_h (bf16
+// pairs, 64 columns) is written over the first half of S_h once the softmax
+// has read S_h.
+constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-
-// shared memory layout (offsets from a 1024-aligned base)
-constexpr int kOffQ = 0;                              // Q0, Q1
-constexpr int kOffP = kOffQ + 2 * kTileBytes;         // P0, P1
-constexpr int kOffRing = kOffP + 2 * kTileBytes;      // 3 slots
-constexpr int kOffBar = kOffRing + kRing * kTileBytes;
-// q_full, q_empty, ring_full[3], ring_empty[3], s_full[2], p_full[2],
-// pv_done[2], o_free[2], s_free[2], grp_sync[2]
-constexpr int kNumBars = 20;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;      // tmem slot, abort flag
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;      // + slack for 1024 alignment
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, /*b_mn_major=*/false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kHeadDim, /*b_mn_major=*/true);
+constexpr int kMaxDynSmem = 232448;  // 227 KB opt-in limit per block
+
+// D[tmem] (+)= A[tmem] * B[smem desc]: the A operand (M x K, bf16) is read
+// from tensor memory, row m in lane m, two consecutive K elements packed per
+// 32-bit column, so one K = 16 step spans 8 columns. Only A may come from
+// tensor memory.
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane (warp-collective).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -113,6 +132,76 @@ __device__ __forceinline__ float softmax_row_to_p(const uint32_t (&sr)[128], flo
   unpack_f32x2(acc0, a, b);
   unpack_f32x2(acc1, c, d);
   return (a + b) + (c + d);
+}
+
+// The same row with P written to tensor memory: bf16 pairs into 64 columns of
+// this thread's TMEM lane starting at t_p (keys 2c and 2c + 1 in column c,
+// the A-operand layout of a PV product read from tensor memory); returns the
+// row's sum of P in fp32. A row with every column masked (-inf) writes a zero
+// P row. Every lane of the warp must call it (the TMEM store is
+// warp-collective).
+__device__ __forceinline__ float softmax_row_to_tmem(const uint32_t (&sr)[128], float qscale,
+                                                     float neg_m, uint32_t t_p) {
+  const unsigned long long qs2 = pack_f32x2(qscale, qscale);
+  const unsigned long long nm2 = pack_f32x2(neg_m, neg_m);
+  unsigned long long acc0 = 0ull, acc1 = 0ull;  // two paired partial sums (0.0f, 0.0f)
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {  // 32 keys -> 16 columns
+    uint32_t pk[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int k0 = 32 * c + 8 * q;
+      float e[8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const unsigned long long x2 = ffma2(
+            pack_f32x2(__uint_as_float(sr[k0 + 2 * u]), __uint_as_float(sr[k0 + 2 * u + 1])),
+            qs2, nm2);
+        float x0, x1;
+        unpack_f32x2(x2, x0, x1);
+        e[2 * u] = ex2(x0);
+        e[2 * u + 1] = ex2(x1);
+      }
+      acc0 = fadd2(acc0, fadd2(pack_f32x2(e[0], e[1]), pack_f32x2(e[2], e[3])));
+      acc1 = fadd2(acc1, fadd2(pack_f32x2(e[4], e[5]), pack_f32x2(e[6], e[7])));
+#pragma unroll
+      for (int u = 0; u < 4; ++u) pk[4 * q + u] = pack_bf16x2(e[2 * u], e[2 * u + 1]);
+    }
+    tmem_st16(t_p + 16 * c, pk);
+  }
+  float a, b, c, d;
+  unpack_f32x2(acc0, a, b);
+  unpack_f32x2(acc1, c, d);
+  return (a + b) + (c + d);
+}
+
+// The epilogue of one row: O / l from this thread's TMEM lane (columns t_o ..
+// t_o + 127) as bf16 into orow (zeros when `has` is false), 32 head dims at a
+// time, straight from registers to global memory. Every lane of the warp must
+// call it (the TMEM loads are warp-collective); only lanes with `store` set
+// write.
+__device__ __forceinline__ void store_o_row(__nv_bfloat16* orow, uint32_t t_o, float inv,
+                                            bool has, bool store) {
+#pragma unroll
+  for (int c = 0; c < kHeadDim; c += 32) {
+    uint32_t o[32];
+    tmem_ld32(t_o + c, o);
+    tmem_wait_ld();
+    if (store) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (has) {
+          const int e = 8 * q;
+          w.x = pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+          w.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+          w.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+          w.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+        }
+        reinterpret_cast<uint4*>(orow + c)[q] = w;
+      }
+    }
+  }
 }
 
 // Bounded wait that also gives up when another role has aborted.

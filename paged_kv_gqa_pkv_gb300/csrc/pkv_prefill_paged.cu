@@ -10,12 +10,24 @@
 // sees its own chunk up to itself. Tokens need no particular order: a decode
 // token is a chunk of one.
 //
-// The kernel keeps the packed prefill's structure (pkv_prefill.cu): a
-// persistent grid walks items of one 128-row query tile x two query heads of
-// a GQA group; warp 0 loads Q and a 3-slot ring of 128-key K/V tiles by TMA,
-// warp 1 issues the tcgen05 MMAs (S = Q K^T and O += P V in TMEM), warps 2..9
-// run the masked online softmax, one row per thread, and the epilogue. What
-// changes is where the keys come from:
+// The kernel keeps the packed prefill's roles (pkv_prefill.cu): a persistent
+// grid walks items of one 128-row query tile x two query heads of a GQA
+// group; warp 0 loads Q and a 5-slot ring of 128-key K/V tiles by TMA, warp 1
+// issues the tcgen05 MMAs, warps 2..9 run the masked online softmax, one row
+// per thread, and the epilogue. Two things differ in the tile loop:
+//  * P stays in tensor memory: the softmax writes it as bf16 pairs over the
+//    first half of S_h, and O_h += P_h V reads its A operand from there, so
+//    the PV product reads only V from shared memory (the packed kernel writes
+//    P to shared memory and the product reads it back). Because P_h sits on
+//    S_h, the next tile's S_h is issued only after that PV has completed;
+//    the two heads' chains (QK, softmax, PV) interleave on the tensor pipe.
+//    This pays on the long key ranges of chunks over a cached prefix (561 ->
+//    488 us on 16 chunks of 512 over prefixes U[512, 4096]); on the packed
+//    workload's short documents, with a few key tiles per item, the serial
+//    chain is exposed and the packed kernel keeps P in shared memory;
+//  * output rows go straight from registers to global memory, and the
+//    shared memory this frees deepens the K/V ring from 3 to 5 slots.
+// What changes otherwise is where the keys come from:
 //  * the rows of a query tile fall into runs of equal batch slot (ballots
 //    over the tile's slots); a run with slot s whose largest position is M
 //    reads the logical key tiles j = 0..M/128 of slot s;
@@ -38,6 +50,20 @@ namespace pkv {
 namespace {
 
 using namespace prefill_detail;
+
+// shared memory layout (offsets from a 1024-aligned base). P lives in tensor
+// memory and the output rows are written straight from registers, so all but
+// Q is K/V ring.
+constexpr int kRing = 5;                              // K/V tile slots
+constexpr int kOffQ = 0;                              // Q0, Q1
+constexpr int kOffRing = kOffQ + 2 * kTileBytes;      // kRing slots
+constexpr int kOffBar = kOffRing + kRing * kTileBytes;
+// q_full, q_empty, ring_full[kRing], ring_empty[kRing], s_full[2], p_full[2],
+// pv_done[2], o_free[2]
+constexpr int kNumBars = 2 + 2 * kRing + 8;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;      // tmem slot, abort flag
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;      // + slack for 1024 alignment
+static_assert(kSmemBytes <= kMaxDynSmem, "shared memory above the opt-in limit");
 
 struct PagedPrefillParams {
   const int32_t* page_table;
@@ -197,7 +223,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
                              const __grid_constant__ CUtensorMap kmap,
                              const __grid_constant__ CUtensorMap vmap,
-                             const __grid_constant__ CUtensorMap omap,
                              const PagedPrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -205,14 +230,12 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* ring_full = bars + 2;   // [3]
-  uint64_t* ring_empty = bars + 5;  // [3]
-  uint64_t* s_full = bars + 8;      // [2]
-  uint64_t* p_full = bars + 10;     // [2]
-  uint64_t* pv_done = bars + 12;    // [2]
-  uint64_t* o_free = bars + 14;     // [2]
-  uint64_t* s_free = bars + 16;     // [2]
-  uint64_t* grp_sync = bars + 18;   // [2]
+  uint64_t* ring_full = bars + 2;               // [kRing]
+  uint64_t* ring_empty = bars + 2 + kRing;      // [kRing]
+  uint64_t* s_full = bars + 2 + 2 * kRing;      // [2]
+  uint64_t* p_full = s_full + 2;                // [2]: P_h in TMEM, O_h rescaled
+  uint64_t* pv_done = s_full + 4;               // [2]
+  uint64_t* o_free = s_full + 6;                // [2]: epilogue has read O_h
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
 
@@ -233,8 +256,6 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
       mbar_init(&p_full[h], kGroupThreads);
       mbar_init(&pv_done[h], 1);
       mbar_init(&o_free[h], kGroupThreads);
-      mbar_init(&s_free[h], kGroupThreads);
-      mbar_init(&grp_sync[h], kGroupThreads);
     }
     *s_abort = (p.dev_err != nullptr &&
                 (*reinterpret_cast<volatile int32_t*>(p.dev_err) & PKV_DEV_ERR_TIMEOUT)) ? 1 : 0;
@@ -244,7 +265,6 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
     tma_prefetch_desc(&qmap);
     tma_prefetch_desc(&kmap);
     tma_prefetch_desc(&vmap);
-    tma_prefetch_desc(&omap);
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
   __syncthreads();
@@ -345,7 +365,6 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
     uint32_t qi = 0;      // non-empty items
     uint32_t tc = 0;      // KV tiles processed (all items)
     const uint32_t sQ = smem_u32(smem + kOffQ);
-    const uint32_t sP = smem_u32(smem + kOffP);
     const uint32_t sR = smem_u32(smem + kOffRing);
     auto qk = [&](int h, uint32_t kslot) {
       const uint32_t q = sQ + h * kTileBytes;
@@ -360,27 +379,14 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
       umma_commit(&s_full[h]);
     };
     auto pv = [&](int h, uint32_t vslot, bool accumulate) {
-      const uint32_t pp = sP + h * kTileBytes;
+      const uint32_t a = tmem + static_cast<uint32_t>(h * kBN);             // P_h, over S_h
       const uint32_t v = sR + vslot * kTileBytes;
       const uint32_t d = tmem + static_cast<uint32_t>(256 + h * kHeadDim);  // O_h
 #pragma unroll
-      for (int kk = 0; kk < kBN / 16; ++kk) {
-        const uint32_t a_off = (kk >> 2) * kHalf + (kk & 3) * 32;
-        umma_bf16(d, sw128_desc(pp + a_off, 0, 1024), sw128_desc(v + kk * 2048, kHalf, 1024),
-                  kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
-      }
+      for (int kk = 0; kk < kBN / 16; ++kk)
+        umma_bf16_ts(d, a + kk * 8, sw128_desc(v + kk * 2048, kHalf, 1024), kIdescPV,
+                     (accumulate || kk > 0) ? 1u : 0u);
       umma_commit(&pv_done[h]);
-    };
-    // QK of one tile for every head of the item; S_h must have been read by
-    // the softmax of the previous tile (global tile count t). Lane 0 only.
-    auto qk_all = [&](uint32_t kslot, uint32_t t) -> bool {
-      for (int h = 0; h < hpi; ++h) {
-        if (t > 0 && !wait_or_abort(&s_free[h], (t - 1) & 1, s_abort)) return false;
-        tc_fence_after();
-        qk(h, kslot);
-      }
-      umma_commit(&ring_empty[kslot]);
-      return true;
     };
     TileRows nxt = tile_rows_load(p, item_r0(p, blockIdx.x, items_per_tile), lane);
     for (int item = blockIdx.x; item < p.n_items && !*s_abort; item += gridDim.x) {
@@ -392,36 +398,37 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
       RunCursor vc;
       cursor_first(vc, cur, rm, lane);
       bool ok = true;
-      uint32_t kslot = C % kRing;
+      const uint32_t k0slot = C % kRing;
       if (lane == 0) {
         ok = wait_or_abort(q_full, qi & 1, s_abort) &&
-             wait_or_abort(&ring_full[kslot], (C / kRing) & 1, s_abort);
-        if (ok) {
+             wait_or_abort(&ring_full[k0slot], (C / kRing) & 1, s_abort);
+        // S_h is free once the previous item's last PV_h has read P_h from it
+        for (int h = 0; ok && h < hpi; ++h) {
+          if (tc > 0 && !wait_or_abort(&pv_done[h], (tc - 1) & 1, s_abort)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          ok = qk_all(kslot, tc);
-          if (ok && n_kv == 1) umma_commit(q_empty);
+          qk(h, k0slot);
+        }
+        if (ok) {
+          umma_commit(&ring_empty[k0slot]);
+          if (n_kv == 1) umma_commit(q_empty);
         }
       }
       ++C;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       for (int t = 0; ok && t < n_kv; ++t) {
-        if (t + 1 < n_kv) {
-          // K_{t+1}: S of the next tile while this tile's softmax runs
-          kslot = C % kRing;
-          if (lane == 0) {
-            ok = wait_or_abort(&ring_full[kslot], (C / kRing) & 1, s_abort) &&
-                 qk_all(kslot, tc + 1);
-            if (ok && t + 2 == n_kv) umma_commit(q_empty);
-          }
-          ++C;
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
-        }
-        const uint32_t vslot = C % kRing;
-        ++C;
+        // ring order: K_{t+1} (if any), then V_t
+        const bool more = t + 1 < n_kv;
+        const uint32_t ck = C;
+        if (more) ++C;
+        const uint32_t cv = C++;
+        const uint32_t kslot = ck % kRing;
+        const uint32_t vslot = cv % kRing;
         // the V tile has landed: zero its rows past the run's last key
         if (!__all_sync(0xffffffffu,
-                        wait_or_abort(&ring_full[vslot], ((C - 1) / kRing) & 1, s_abort))) {
+                        wait_or_abort(&ring_full[vslot], (cv / kRing) & 1, s_abort))) {
           ok = false;
           break;
         }
@@ -439,6 +446,7 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
         }
         __syncwarp();
         if (lane == 0) {
+          if (more && !wait_or_abort(&ring_full[kslot], (ck / kRing) & 1, s_abort)) ok = false;
           for (int h = 0; h < hpi && ok; ++h) {
             if (!wait_or_abort(&p_full[h], tc & 1, s_abort)) {
               ok = false;
@@ -450,8 +458,23 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
             }
             tc_fence_after();
             pv(h, vslot, t > 0);
+            if (more) {
+              // the next S_h overwrites P_h: wait until this PV has read it
+              if (!wait_or_abort(&pv_done[h], tc & 1, s_abort)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              qk(h, kslot);
+            }
           }
-          if (ok) umma_commit(&ring_empty[vslot]);
+          if (ok) {
+            umma_commit(&ring_empty[vslot]);
+            if (more) {
+              umma_commit(&ring_empty[kslot]);
+              if (t + 2 == n_kv) umma_commit(q_empty);
+            }
+          }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         ++tc;
@@ -468,15 +491,7 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
     const int row = lane_base + lane;
     const uint32_t t_s = tmem + (static_cast<uint32_t>(lane_base) << 16) + grp * kBN;
     const uint32_t t_o = tmem + (static_cast<uint32_t>(lane_base) << 16) + 256 + grp * kHeadDim;
-    uint8_t* sP = smem + kOffP + grp * kTileBytes;
-    const bool store_thread = (warp & 3) == 2 && lane == 0;  // first warp of the group
-    uint32_t tc = 0, qi = 0, gs = 0;
-    auto group_sync = [&]() -> bool {
-      mbar_arrive(&grp_sync[grp]);
-      const bool w = wait_or_abort(&grp_sync[grp], gs & 1, s_abort);
-      ++gs;
-      return __all_sync(0xffffffffu, w);
-    };
+    uint32_t tc = 0, qi = 0;
     const bool active = grp < hpi;
     TileRows nxt = tile_rows_load(p, item_r0(p, blockIdx.x, items_per_tile), lane);
     for (int item = blockIdx.x; active && item < p.n_items; item += gridDim.x) {
@@ -515,26 +530,24 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
           tmem_ld32(t_s + 96, d);
           tmem_wait_ld();
         }
-        tc_fence_before();
-        mbar_arrive(&s_free[grp]);
         // this row sees key tile j of its own run, columns 0 .. pos - 128j
         const bool in_run = row >= c.s && row < c.e;
         const int c_hi = in_run ? min(my_pos - c.j * kBN, kBN - 1) : -1;
-        const bool none = c_hi < 0;
         const bool full = c_hi == kBN - 1;
         cursor_next(c, cur, rm, lane);
-        float mx = -INFINITY;
-        if (!none) {
+        // masked columns become -inf (all of them when nothing is visible, c_hi
+        // < 0), so every lane takes the same P path (the TMEM store is
+        // warp-collective)
+        float mx;
+        if (full) {
+          mx = row_max_full(sr);
+        } else {
           float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-          if (full) {
-            m4[0] = row_max_full(sr);
-          } else {
 #pragma unroll
-            for (int q = 0; q < kBN; ++q) {
-              const float v = q <= c_hi ? __uint_as_float(sr[q]) : -INFINITY;
-              sr[q] = __float_as_uint(v);
-              m4[q & 3] = fmaxf(m4[q & 3], v);
-            }
+          for (int q = 0; q < kBN; ++q) {
+            const float v = q <= c_hi ? __uint_as_float(sr[q]) : -INFINITY;
+            sr[q] = __float_as_uint(v);
+            m4[q & 3] = fmaxf(m4[q & 3], v);
           }
           mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         }
@@ -551,22 +564,8 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
           break;
         }
         tc_fence_after();
-        if (j == 0) {
-          if (store_thread) bulk_wait_read_all();
-          if (!group_sync()) {
-            ok = false;
-            break;
-          }
-        }
-        float psum = 0.f;
-        if (none) {
-#pragma unroll
-          for (int q = 0; q < 16; ++q)
-            *reinterpret_cast<uint4*>(sP + (q >> 3) * kHalf + row * 128 +
-                                      (((q & 7) ^ (row & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
-        } else {
-          psum = softmax_row_to_p(sr, p.qscale, neg_m, sP, row);
-        }
+        // P over the first 64 columns of S_h (already in registers)
+        const float psum = softmax_row_to_tmem(sr, p.qscale, neg_m, t_s);
         l_run = l_run * alpha + psum;
         m_run = m_use;
         if (j > 0 && __any_sync(0xffffffffu, grow)) {
@@ -579,9 +578,8 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
             for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
             tmem_st32(t_o + q, o);
           }
-          tmem_wait_st();
         }
-        fence_proxy_async_smem();
+        tmem_wait_st();
         tc_fence_before();
         mbar_arrive(&p_full[grp]);
         ++tc;
@@ -595,43 +593,14 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
       const bool in_range = i < p.n_tokens;
       const bool has = in_range && my_b != 0 && ok && l_run > 0.f;
       const float inv = has ? 1.f / l_run : 0.f;
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
+                            (static_cast<int64_t>(i) * p.num_q_heads + head) * kHeadDim;
       if (n_kv > 0 && ok) {
-        uint32_t o[128];
-        {
-          uint32_t (&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(&o[0]);
-          uint32_t (&b)[32] = *reinterpret_cast<uint32_t(*)[32]>(&o[32]);
-          uint32_t (&cc)[32] = *reinterpret_cast<uint32_t(*)[32]>(&o[64]);
-          uint32_t (&d)[32] = *reinterpret_cast<uint32_t(*)[32]>(&o[96]);
-          tmem_ld32(t_o + 0, a);
-          tmem_ld32(t_o + 32, b);
-          tmem_ld32(t_o + 64, cc);
-          tmem_ld32(t_o + 96, d);
-          tmem_wait_ld();
-        }
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          uint4 w = make_uint4(0u, 0u, 0u, 0u);
-          if (has) {
-            const int e = 8 * q;
-            w.x = pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-          }
-          *reinterpret_cast<uint4*>(sP + (q >> 3) * kHalf + row * 128 +
-                                    (((q & 7) ^ (row & 7)) << 4)) = w;
-        }
-        fence_proxy_async_smem();
-        const bool synced = group_sync();
-        if (synced && store_thread) {
-          tma_store_3d(&omap, sP, 0, head, r0);
-          tma_store_3d(&omap, sP + kHalf, 64, head, r0);
-          bulk_commit_group();
-        }
-        if (!synced) ok = false;
+        // O / l as bf16 straight from TMEM to this row of the output (the
+        // item's last PV has completed)
+        store_o_row(orow, t_o, inv, has, in_range);
       } else if (in_range) {
-        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
-                              (static_cast<int64_t>(i) * p.num_q_heads + head) * kHeadDim;
+        // no key tile at all (padding-only tile) or an aborted item: zeros
 #pragma unroll
         for (int q = 0; q < kHeadDim; q += 8)
           *reinterpret_cast<uint4*>(orow + q) = make_uint4(0u, 0u, 0u, 0u);
@@ -651,7 +620,6 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
       }
     }
   }
-  if (warp >= 2 && (warp & 3) == 2 && lane == 0) bulk_wait_all();  // output stores done
   if (*s_abort && threadIdx.x == 0) set_dev_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
   tc_fence_before();
   __syncthreads();
@@ -718,11 +686,10 @@ pkv_status prefill_paged_entry(const pkv_cache_desc* cache, const void* k_pool,
     return PKV_ERR_ARG;
   const int box_rows = ps < kBN ? ps : kBN;
 
-  CUtensorMap qmap, kmap, vmap, omap;
+  CUtensorMap qmap, kmap, vmap;
   if (!encode_packed_map(&qmap, q, num_q_heads, n_tokens) ||
       !encode_pool_box_map(&kmap, k_pool, cache, box_rows) ||
-      !encode_pool_box_map(&vmap, v_pool, cache, box_rows) ||
-      !encode_packed_map(&omap, out, num_q_heads, n_tokens))
+      !encode_pool_box_map(&vmap, v_pool, cache, box_rows))
     return PKV_ERR_ARG;
 
   static bool attr_set[64] = {};
@@ -757,7 +724,7 @@ pkv_status prefill_paged_entry(const pkv_cache_desc* cache, const void* k_pool,
   prm.qscale = scale * 1.4426950408889634f;
   const int grid = prm.n_items < sms ? prm.n_items : sms;
   const cudaError_t e = launch_kernel(prefill_paged_tcgen05_kernel, dim3(grid), dim3(kThreads),
-                                      kSmemBytes, stream, false, qmap, kmap, vmap, omap, prm);
+                                      kSmemBytes, stream, false, qmap, kmap, vmap, prm);
   return record_cuda_status(e);
 }
 
