@@ -526,6 +526,70 @@ def run_pkv(args):
                 "peak_kind": peak_kind,
                 "traffic": captured_traffic("chunked_prefill_call") if n_decode == 0 else None}
 
+    def timed_mixed_split(reps, n_decode=48):
+        """The same mixed step (16 chunks of 512 plus `n_decode` one-token
+        decodes, shuffled) served as two calls: the chunks' tokens through the
+        paged prefill (their K/V appended once beforehand), and the decode
+        tokens through the fused append + split-KV decode. Each call and the
+        pair are timed with CUDA events over `reps` back-to-back repetitions."""
+        c = W.chunked_prefill(0, n_decode=n_decode)
+        slot_len = {s + 1: n for s, n in enumerate(c.chunk_lens)}
+        is_dec = torch.tensor([slot_len.get(int(b), 0) == 1 for b in c.batch_idx.tolist()])
+        ci = (~is_dec).nonzero().flatten()
+        di = is_dec.nonzero().flatten()
+        kp, vp, pt = c.k_pool.to(dev), c.v_pool.to(dev), c.page_table.to(dev)
+        q_c, bi_c, ip_c = c.q[ci].to(dev), c.batch_idx[ci].to(dev), c.input_pos[ci].to(dev)
+        q_d, bi_d = c.q[di].to(dev), c.batch_idx[di].to(dev)
+        sl_d = (c.input_pos[di] + 1).to(dev)
+        kn_d, vn_d = c.k_new[di].to(dev), c.v_new[di].to(dev)
+        nd = int(di.numel())
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        binding.pkv_append(kp, vp, pt, c.k_new[ci].to(dev), c.v_new[ci].to(dev), bi_c, ip_c,
+                           c.page_size, dev_err=err)
+        out_c = torch.empty_like(q_c)
+        lse_c = torch.empty((q_c.shape[0], c.num_q_heads), dtype=torch.float32, device=dev)
+        out_d = torch.empty_like(q_d)
+        lse_d = torch.empty((nd, c.num_q_heads), dtype=torch.float32, device=dev)
+        ws = torch.empty(binding.pkv_decode_workspace_size(kp, pt, c.page_size, nd,
+                                                           c.num_q_heads),
+                         dtype=torch.uint8, device=dev)
+
+        def pre():
+            binding.pkv_prefill_paged_attention(kp, vp, pt, q_c, bi_c, ip_c, c.page_size,
+                                                c.scale, out=out_c, lse=lse_c, dev_err=err)
+
+        def dec():
+            binding.pkv_decode_append_attention(kp, vp, pt, q_d, kn_d, vn_d, bi_d, sl_d,
+                                                c.page_size, c.scale, out=out_d, lse=lse_d,
+                                                workspace=ws, dev_err=err)
+        for _ in range(3):
+            pre()
+            dec()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        ev[0].record()
+        for _ in range(reps):
+            pre()
+        ev[1].record()
+        for _ in range(reps):
+            dec()
+        ev[2].record()
+        for _ in range(reps):
+            pre()
+            dec()
+        ev[3].record()
+        torch.cuda.synchronize()
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(err.item()):#x} in the split mixed step")
+        both_us = ev[2].elapsed_time(ev[3]) / reps * 1e3
+        flops = 4.0 * c.head_dim * c.num_q_heads * c.info["pairs"]
+        tf = flops / (both_us * 1e-6) / 1e12
+        return {"prefill_call_us": ev[0].elapsed_time(ev[1]) / reps * 1e3,
+                "decode_call_us": ev[1].elapsed_time(ev[2]) / reps * 1e3,
+                "step_us": both_us, "tflops": tf, "frac": tf / bf16_peak,
+                "calls": "pkv_prefill_paged_attention on the chunks' tokens, then "
+                         f"pkv_decode_append_attention on the {nd} decode tokens"}
+
     from paged_kv_gqa_pkv_gb300 import sharding
     # each rank serves its own shard of independent sequences (weak scaling)
     case = W.qwen3_b64_decode(sharding.shard_seed(rank), permute=False)
@@ -551,7 +615,7 @@ def run_pkv(args):
     mixed = timed_chunked_prefill(20, n_decode=48)
     chunked["mixed_step_with_48_decode_tokens"] = {
         "attention_call_us": mixed["attention_call_us"], "tflops": mixed["tflops"],
-        "frac": mixed["frac"]}
+        "frac": mixed["frac"], "split": timed_mixed_split(20)}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
