@@ -99,3 +99,21 @@ def test_bad_page_for_new_token_is_flagged_other_rows_exact():
     assert bad_tok == [1] and bad_rows == [1]
     assert np.array_equal(bf16_bits(kp), ek) and np.array_equal(bf16_bits(vp), ev)
     assert_attention_close(out, lse, ref_o, ref_l, rows=[0, 2])
+
+
+@pytest.mark.parametrize("ps", [48, 256])
+def test_fused_other_page_sizes(ps):
+    """The new token's slot through the page table for page sizes that are
+    not 128: pools bit-exact, attention against the oracle, and the same bits
+    as the two-call step."""
+    lens = [1, 16, ps, ps + 1, 2 * ps - 1, 500]
+    c = W.custom_decode(33, lens, hq=32, hkv=8, page_size=ps, permute=True)
+    kp, vp, out, lse, err = run_fused(c)
+    ek, ev, ref_o, ref_l, bad_tok, bad_rows = oracle_decode_step(c)
+    assert err == 0 and not bad_tok and not bad_rows
+    assert np.array_equal(bf16_bits(kp), ek) and np.array_equal(bf16_bits(vp), ev)
+    assert_attention_close(out, lse, ref_o, ref_l, tag=f"fused ps={ps}")
+    k2, v2, o2, l2, e2 = run_decode_step(c)
+    assert e2 == 0
+    assert torch.equal(kp, k2) and torch.equal(vp, v2)
+    assert torch.equal(out, o2) and torch.equal(lse, l2)

@@ -212,3 +212,15 @@ def test_long_rows_small_batch_combined_per_cta(lens, hq, hkv, ps):
     for small batch x kv heads)."""
     c = W.custom_decode(29, lens, hq=hq, hkv=hkv, page_size=ps, permute=True)
     _full_parity(c)
+
+
+@pytest.mark.parametrize("ps,permute", [(48, True), (48, False), (80, True), (256, True),
+                                        (256, False)],
+                         ids=["ps48_perm", "ps48_seq", "ps80_perm", "ps256_perm", "ps256_seq"])
+def test_page_sizes_that_are_not_powers_of_two_or_above_a_tile_row(ps, permute):
+    """Any multiple of 16 is a valid page size: lengths on both sides of tile
+    (16) and page edges, over permuted pages (table walk) and sequential ones
+    (contiguous fast path)."""
+    lens = [1, 15, 16, 17, ps - 1, ps, ps + 1, 2 * ps + 16, 3 * ps + 5, 700]
+    c = W.custom_decode(31, lens, hq=32, hkv=8, page_size=ps, permute=permute)
+    _full_parity(c)
