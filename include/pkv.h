@@ -165,6 +165,10 @@ size_t pkv_decode_workspace_size(const pkv_cache_desc* cache, int batch,
  * n > max_blocks * page_size (or n < 0) sets a PKV_DEV_ERR bit and gives
  * 0 / -inf; a page entry out of range within the first n keys sets
  * PKV_DEV_ERR_BAD_PAGE and leaves that row unspecified.
+ * out and lse are only written, with plain stores (no bulk copies): besides
+ * device memory they may be pinned host memory mapped into the device's
+ * address space (unified addressing), so that the results land on the host
+ * without a separate copy; the caller synchronises the stream before reading.
  *
  * workspace: device scratch of at least pkv_decode_workspace_size() bytes,
  * 256-byte aligned, owned by the caller; its contents need no initialisation

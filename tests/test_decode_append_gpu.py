@@ -117,3 +117,20 @@ def test_fused_other_page_sizes(ps):
     assert e2 == 0
     assert torch.equal(kp, k2) and torch.equal(vp, v2)
     assert torch.equal(out, o2) and torch.equal(lse, l2)
+
+
+def test_results_written_straight_into_pinned_host_memory():
+    """out and lse may be pinned host memory (the kernels write them with
+    plain stores): the same bits as device buffers, with no copy."""
+    c = W.qwen3_b64_decode(2, permute=True)
+    k1, v1, o1, l1, e1 = run_fused(c)
+    kp, vp = gpu(c.k_pool), gpu(c.v_pool)
+    out_h = torch.zeros((c.batch, c.num_q_heads, c.head_dim), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.zeros((c.batch, c.num_q_heads), dtype=torch.float32).pin_memory()
+    err = new_dev_err()
+    binding.pkv_decode_append_attention(kp, vp, gpu(c.page_table), gpu(c.q), gpu(c.k_new),
+                                        gpu(c.v_new), gpu(c.batch_idx), gpu(c.seq_lens),
+                                        c.page_size, c.scale, out=out_h, lse=lse_h, dev_err=err)
+    torch.cuda.synchronize()
+    assert e1 == 0 and int(err.item()) == 0
+    assert torch.equal(out_h, o1) and torch.equal(lse_h, l1)
