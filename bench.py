@@ -475,6 +475,26 @@ def run_pkv(args):
             raise RuntimeError(f"device error bits {int(err.item()):#x} in prefill")
         app_us = ev[0].elapsed_time(ev[1]) / reps * 1e3
         att_us = ev[1].elapsed_time(ev[2]) / reps * 1e3
+        # the same append with k_norm and the rotary embedding applied to K
+        # (Qwen3's rope theta 1e6; a seeded k_norm weight)
+        cos, sin = W.rope_tables(int(c.input_pos.max()) + 1)
+        cos, sin = cos.to(dev), sin.to(dev)
+        knw = (torch.rand(c.head_dim, generator=torch.Generator().manual_seed(0)) * 1.75
+               + 0.25).to(dev)
+        for _ in range(3):
+            binding.pkv_append_rope(kp, vp, pt, k, v, bi, ip, c.page_size, cos, sin,
+                                    k_norm_weight=knw, dev_err=err)
+        torch.cuda.synchronize()
+        er = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        er[0].record()
+        for _ in range(reps):
+            binding.pkv_append_rope(kp, vp, pt, k, v, bi, ip, c.page_size, cos, sin,
+                                    k_norm_weight=knw, dev_err=err)
+        er[1].record()
+        torch.cuda.synchronize()
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(err.item()):#x} in the rope append")
+        rope_us = er[0].elapsed_time(er[1]) / reps * 1e3
         flops = 4.0 * c.head_dim * c.num_q_heads * c.info["pairs"]
         tf = flops / (att_us * 1e-6) / 1e12
         return {"workload": f"packed_prefill: 64 documents, lengths U[64,1024], "
@@ -485,7 +505,10 @@ def run_pkv(args):
                 "traffic": captured_traffic("prefill_call"),
                 "append_call_us": app_us,
                 "append_gbs": (c.n_tokens * c.num_kv_heads * c.head_dim * 2 * 4)
-                / (app_us * 1e-6) / 1e9}
+                / (app_us * 1e-6) / 1e9,
+                "append_rope_knorm_call_us": rope_us,
+                "append_rope_knorm_gbs": (c.n_tokens * c.num_kv_heads * c.head_dim * 2 * 4)
+                / (rope_us * 1e-6) / 1e9}
 
     def timed_chunked_prefill(reps, n_decode=0):
         """Chunked prefill over the paged cache: 16 chunks of 512 tokens over
