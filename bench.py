@@ -510,13 +510,13 @@ def run_pkv(args):
                 "append_rope_knorm_gbs": (c.n_tokens * c.num_kv_heads * c.head_dim * 2 * 4)
                 / (rope_us * 1e-6) / 1e9}
 
-    def timed_chunked_prefill(reps, n_decode=0):
+    def timed_chunked_prefill(reps, n_decode=0, page_size=128):
         """Chunked prefill over the paged cache: 16 chunks of 512 tokens over
         prefixes U[512, 4096] (T=8192), pages permuted, plus `n_decode` decode
         tokens for a mixed step. The chunk K/V are appended once; the tcgen05
         paged attention is timed with CUDA events over `reps` back-to-back
         calls (the pools, ~450 MB, exceed L2)."""
-        c = W.chunked_prefill(0, n_decode=n_decode)
+        c = W.chunked_prefill(0, n_decode=n_decode, page_size=page_size)
         q, bi, ip = c.q.to(dev), c.batch_idx.to(dev), c.input_pos.to(dev)
         kp, vp, pt = c.k_pool.to(dev), c.v_pool.to(dev), c.page_table.to(dev)
         out = torch.empty_like(q)
@@ -542,11 +542,12 @@ def run_pkv(args):
         tf = flops / (att_us * 1e-6) / 1e12
         return {"workload": f"chunked_prefill: 16 chunks of 512 over prefixes U[512,4096] + "
                             f"{n_decode} decode tokens, T={c.n_tokens}, Hq=32, Hkv=8, D=128, "
-                            f"page 128, permuted pages, seed 0",
+                            f"page {page_size}, permuted pages, seed 0",
                 "attention_call_us": att_us, "algorithmic_flops": flops, "tflops": tf,
                 "bound": "tensor", "peak_tflops": bf16_peak, "frac": tf / bf16_peak,
                 "peak_kind": peak_kind,
-                "traffic": captured_traffic("chunked_prefill_call") if n_decode == 0 else None}
+                "traffic": (captured_traffic("chunked_prefill_call")
+                            if n_decode == 0 and page_size == 128 else None)}
 
     def timed_mixed_split(reps, n_decode=48):
         """The same mixed step (16 chunks of 512 plus `n_decode` one-token
@@ -631,10 +632,13 @@ def run_pkv(args):
     dec_gbs = bytes_dec / (r["dec_ms"] * 1e-3) / 1e9
     perm = W.qwen3_b64_decode(0, permute=True)
     rp = timed_decode(perm, max(args.steps // 4, 10), args.warmup)
+    perm256 = W.qwen3_b64_decode(0, permute=True, page_size=256)
+    rp256 = timed_decode(perm256, max(args.steps // 4, 10), args.warmup)
     e2e_ms, h2d, d2h = e2e_decode(case, max(args.steps // 10, 10), args.warmup)
     prefill = timed_prefill(20)
     chunked = timed_chunked_prefill(20)
     mixed = timed_chunked_prefill(20, n_decode=48)
+    chunked256 = timed_chunked_prefill(20, page_size=256)
     chunked["mixed_step_with_48_decode_tokens"] = {
         "attention_call_us": mixed["attention_call_us"], "tflops": mixed["tflops"],
         "frac": mixed["frac"], "split": timed_mixed_split(20)}
@@ -660,6 +664,13 @@ def run_pkv(args):
                                "append, then the LSE merge): the timed step",
                      "algorithmic_bytes": step_bytes(case),
                      "peak_kind": peak_kind, "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS},
+        "page_size_256": {
+            "decode_call_us": rp256["dec_ms"] * 1e3,
+            "decode_frac": decode_bytes(perm256) / (rp256["dec_ms"] * 1e-3) / 1e9 / hbm_peak,
+            "chunked_prefill_call_us": chunked256["attention_call_us"],
+            "chunked_prefill_frac": chunked256["frac"],
+            "workloads": "qwen3_b64_decode and chunked_prefill as above, page 256, "
+                         "permuted pages"},
         "permuted_pages": {"decode_call_us": rp["dec_ms"] * 1e3,
                            "achieved_gbs": decode_bytes(perm) / (rp["dec_ms"] * 1e-3) / 1e9,
                            "frac": decode_bytes(perm) / (rp["dec_ms"] * 1e-3) / 1e9 / hbm_peak},

@@ -213,16 +213,18 @@ def tiny_decode(seed: int = 0, permute: bool = True) -> DecodeCase:
                         max_blocks=16)
 
 
-def qwen3_b64_decode(seed: int = 0, permute: bool = False,
-                     batch: int = 64) -> DecodeCase:
-    """Qwen3-4B-shaped decode, one layer: B=64, Hq=32, Hkv=8, page 128, keys
-    attended uniform in [512, 1024]. Sequential pages (contiguous fast path)
-    or a seeded permutation."""
+def qwen3_b64_decode(seed: int = 0, permute: bool = False, batch: int = 64,
+                     page_size: int = 128) -> DecodeCase:
+    """Qwen3-4B-shaped decode, one layer: B=64, Hq=32, Hkv=8, page 128 (or
+    ``page_size``; the pages also ran 256), keys attended uniform in
+    [512, 1024]. Sequential pages (contiguous fast path) or a seeded
+    permutation."""
     gen = torch.Generator().manual_seed(seed)
     lens = torch.randint(512, 1025, (batch,), generator=gen).tolist()
-    return _decode_case(f"qwen3_b{batch}_decode_{'perm' if permute else 'seq'}",
-                        gen, lens=lens, n_pad=0, hq=32, hkv=8, page_size=128,
-                        permute=permute, max_blocks=8)
+    suffix = "" if page_size == 128 else f"_ps{page_size}"
+    return _decode_case(f"qwen3_b{batch}_decode_{'perm' if permute else 'seq'}{suffix}",
+                        gen, lens=lens, n_pad=0, hq=32, hkv=8, page_size=page_size,
+                        permute=permute, max_blocks=(1024 + page_size - 1) // page_size)
 
 
 def padded_bucket_decode(seed: int = 0) -> DecodeCase:
@@ -326,6 +328,9 @@ def chunked_prefill(seed: int = 0, *, prefix_lens=None, chunk_lens=None, n_chunk
     chunk_lens = [int(x) for x in chunk_lens]
     S = len(pre)
     d = HEAD_DIM
+    # the packed order is drawn before anything whose size depends on the
+    # page size, so that page sizes are compared on the same token order
+    order = torch.randperm(S, generator=gen).tolist() if shuffle else list(range(S))
     blocks = [_blocks(p + c, page_size) for p, c in zip(pre, chunk_lens)]
     max_blocks = max(blocks) if blocks else 1
     num_pages = 1 + sum(blocks)
@@ -342,7 +347,6 @@ def chunked_prefill(seed: int = 0, *, prefix_lens=None, chunk_lens=None, n_chunk
                 r = int(table[s + 1, t // page_size]) * page_size + t % page_size
                 k_pool[r] = _randn_bf16((hkv, d), gen)
                 v_pool[r] = _randn_bf16((hkv, d), gen)
-    order = torch.randperm(S, generator=gen).tolist() if shuffle else list(range(S))
     bidx, pos = [], []
     for s in order:
         bidx += [s + 1] * chunk_lens[s]
