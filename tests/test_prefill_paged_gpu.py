@@ -154,3 +154,31 @@ def test_bad_entries_flagged_other_tokens_exact():
     ref_o, ref_l, _, bad = oracle_chunked(c, rows=ok_rows, table=table)
     assert not bad
     assert_attention_close(out, lse, ref_o, ref_l, rows=ok_rows)
+
+
+@pytest.mark.parametrize("offset_elems", [0, 8], ids=["out_32B_aligned", "out_16B_offset"])
+def test_output_alignment_paths(offset_elems):
+    """out needs only 16-byte alignment: a 32-byte-aligned buffer and one at
+    a 16-byte offset both match the oracle, and nothing outside out is
+    written."""
+    c = W.chunked_prefill(5, prefix_lens=[100, 300, 0], chunk_lens=[140, 60, 33], page_size=64,
+                          hq=16, hkv=4)
+    kp, vp, pt = gpu(c.k_pool), gpu(c.v_pool), gpu(c.page_table)
+    bidx, pos = gpu(c.batch_idx), gpu(c.input_pos)
+    err = new_dev_err()
+    binding.pkv_append(kp, vp, pt, gpu(c.k_new), gpu(c.v_new), bidx, pos, c.page_size,
+                       dev_err=err)
+    T, hq, d = c.q.shape
+    buf = torch.full((T * hq * d + 16,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = buf[offset_elems:offset_elems + T * hq * d].view(T, hq, d)
+    assert out.data_ptr() % 32 == (0 if offset_elems == 0 else 16)
+    _, lse = binding.pkv_prefill_paged_attention(kp, vp, pt, gpu(c.q), bidx, pos, c.page_size,
+                                                 c.scale, out=out, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ro, rl, bad_tok, bad = oracle_chunked(c)
+    assert not bad_tok and not bad
+    assert_attention_close(out.cpu(), lse.cpu(), ro, rl, tag=f"out offset {offset_elems}")
+    # nothing written outside out
+    rest = torch.cat([buf[:offset_elems], buf[offset_elems + T * hq * d:]]).cpu()
+    assert torch.isnan(rest.float()).all()
