@@ -265,7 +265,11 @@ pkv_status pkv_decode_attention_static_scratch(
  * 0 / -inf; an unreserved page entry among a token's keys sets
  * PKV_DEV_ERR_BAD_PAGE and leaves that token's result unspecified.
  * page_size must be 16, 32, 64 or a multiple of 128 (PKV_ERR_ARG otherwise);
- * scale must be finite and > 0. The pools are only read.
+ * scale must be finite and > 0. out: bf16 [n_tokens, num_q_heads, D] and
+ * lse: fp32 [n_tokens, num_q_heads], 16- and 4-byte aligned. The pools are
+ * only read. A decode token costs a full 128-row product per key tile of its
+ * prefix here: in a step that mixes chunks and decode tokens, the decode
+ * tokens are cheaper through pkv_decode_append_attention.
  */
 pkv_status pkv_prefill_paged_attention(const pkv_cache_desc* cache, const void* k_pool,
                                        const void* v_pool, const int32_t* page_table,
@@ -289,8 +293,9 @@ pkv_status pkv_prefill_paged_attention(const pkv_cache_desc* cache, const void* 
  * A token that breaks it sets PKV_DEV_ERR_LAYOUT (its row is unspecified).
  * Writes out bf16 [n_tokens, num_q_heads, D] and lse fp32
  * [n_tokens, num_q_heads] with the same formulas as decode; padding tokens
- * give 0 / -inf. scale must be finite and > 0. Writing the k/v into the
- * pages is a separate pkv_append.
+ * give 0 / -inf. scale must be finite and > 0. q, k, v and out are
+ * 16-byte aligned device memory (out is written with bulk tensor stores).
+ * Writing the k/v into the pages is a separate pkv_append.
  */
 pkv_status pkv_prefill_attention(const void* q, const void* k, const void* v,
                                  int num_q_heads, int num_kv_heads,
