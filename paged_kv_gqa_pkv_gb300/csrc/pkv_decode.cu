@@ -43,6 +43,8 @@
 // memory. Keys past a row's length are masked to -inf in S and their V rows
 // are zeroed in shared memory before the fragments are read (stale slots of a
 // page may hold any bits, NaN included).
+#include <atomic>
+
 #include "pkv_launch.h"
 
 namespace pkv {
@@ -812,17 +814,17 @@ static cudaError_t launch_decode_gc(const DecodeParams& p, const CUtensorMap& km
   static_assert(C::smem_bytes(kDecodeMaxBatch) <= 232448, "decode shared memory over budget");
   // The shared-memory opt-in is set once per device, so steady-state calls
   // (and calls under stream capture) only enqueue kernels.
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64] = {};  // per device; host threads may race to set it
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(decode_splitkv_kernel<G, kCombine>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(C::smem_bytes(kDecodeMaxBatch)));
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   e = launch_kernel(decode_splitkv_kernel<G, kCombine>, dim3(sm_count), dim3(kDecodeWarps * 32),
                     smem, stream, /*programmatic=*/true, kmap, vmap, p);

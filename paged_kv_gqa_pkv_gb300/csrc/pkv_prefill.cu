@@ -34,6 +34,7 @@
 // Q, K and P are K-major (64 elements per 128-byte row, two 16 KB halves of
 // D or of the key block); V is used MN-major straight from its TMA tile
 // (64 head dims per 128-byte row, one row per key).
+#include <atomic>
 #include <cmath>
 
 #include "pkv_prefill_common.cuh"
@@ -595,13 +596,13 @@ pkv_status prefill_entry(const void* q, const void* k, const void* v, int num_q_
       !encode_packed_map(&omap, out, num_q_heads, n_tokens))
     return PKV_ERR_ARG;
 
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64] = {};  // per device; host threads may race to set it
   if (dev < 0 || dev >= 64) return PKV_ERR_DEVICE;
-  if (!attr_set[dev]) {
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
     const cudaError_t ea = cudaFuncSetAttribute(
         prefill_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (ea != cudaSuccess) return record_cuda_status(ea);
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)

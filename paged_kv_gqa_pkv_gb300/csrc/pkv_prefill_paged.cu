@@ -41,6 +41,7 @@
 //    their P is zero, but 0 * NaN is not).
 // Every role recomputes the runs from the same tile metadata, so they agree
 // on the key-tile sequence without sharing it through memory.
+#include <atomic>
 #include <cmath>
 
 #include "pkv_prefill_common.cuh"
@@ -692,13 +693,13 @@ pkv_status prefill_paged_entry(const pkv_cache_desc* cache, const void* k_pool,
       !encode_pool_box_map(&vmap, v_pool, cache, box_rows))
     return PKV_ERR_ARG;
 
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64] = {};  // per device; host threads may race to set it
   if (dev < 0 || dev >= 64) return PKV_ERR_DEVICE;
-  if (!attr_set[dev]) {
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
     const cudaError_t ea = cudaFuncSetAttribute(
         prefill_paged_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (ea != cudaSuccess) return record_cuda_status(ea);
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
