@@ -5,10 +5,12 @@ allocated with PyTorch when the caller passes none, and every computation
 runs in the library's CUDA kernels on the caller's current stream. There is
 no fallback: if ``libpkv.so`` is missing or fails to load, every call raises.
 
-Functions keep the names of the C entry points:
-``pkv_append``, ``pkv_decode_attention``, ``pkv_decode_append_attention``,
-``pkv_decode_workspace_size``,
-``pkv_prefill_attention``, ``pkv_status_string``.
+Functions keep the names of the C entry points: ``pkv_append``,
+``pkv_append_rope``, ``pkv_decode_workspace_size``, ``pkv_decode_attention``,
+``pkv_decode_append_attention``, ``pkv_decode_attention_static_scratch``,
+``pkv_prefill_attention``, ``pkv_prefill_paged_attention``,
+``pkv_status_string``, ``pkv_status_from_device_error`` and
+``pkv_last_cuda_error_string``.
 """
 
 from __future__ import annotations
@@ -108,6 +110,18 @@ def status_string(status: int) -> str:
 
 
 pkv_status_string = status_string
+
+
+def pkv_status_from_device_error(dev_err_word: int) -> int:
+    """Status for a dev_err word read back after the stream synchronised:
+    PKV_OK when 0, PKV_ERR_BAD_PAGE when the bad-page bit is set, else
+    PKV_ERR_BAD_INPUT."""
+    return int(load_library().pkv_status_from_device_error(int(dev_err_word)))
+
+
+def pkv_last_cuda_error_string() -> str:
+    """Text of the CUDA error behind the last PKV_ERR_CUDA of this process."""
+    return load_library().pkv_last_cuda_error_string().decode()
 
 
 def _ptr(t: Optional[torch.Tensor]):

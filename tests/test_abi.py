@@ -34,6 +34,13 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, n), f"{n} declared in pkv.h but not exported"
 
 
+def test_binding_has_a_function_of_each_declared_name():
+    """The Python binding keeps the C names: one callable per declared entry
+    point."""
+    for n in _declared():
+        assert callable(getattr(binding, n, None)), f"binding has no {n}"
+
+
 def test_status_strings(lib):
     for s in range(8):
         assert binding.status_string(s) != "unknown status"
