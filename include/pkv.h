@@ -190,7 +190,7 @@ pkv_status pkv_decode_attention(const pkv_cache_desc* cache, const void* k_pool,
  * Source: the pages' decode step writes the new token's K/V into the paged
  * cache, then attends over the cache including it ("qwen3_flex_inference.py",
  * forward "Write to paged KV cache" then flex_attention with
- * _decode_block_mask); fusing the two is the survey's next step after graphs.
+ * _decode_block_mask); fused, a step is one call and one launch fewer.
  *
  * Same arguments and results as pkv_decode_attention, plus k_new, v_new:
  * bf16 [batch, num_kv_heads, D], 16-byte aligned. Row b's new token is
