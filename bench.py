@@ -164,49 +164,78 @@ def _dist():
 
 
 _ORACLE_CHILD = """
-import json, statistics, sys, time
+import json, multiprocessing as mp, os, statistics, sys, time
 sys.path.insert(0, ROOT)
 import oracle.paged_attention as orc
 from paged_kv_gqa_pkv_gb300 import workloads as W
 from paged_kv_gqa_pkv_gb300.workloads import bf16_bits
-c = W.qwen3_b64_decode(0, permute=False)
+c = (W.long_context_decode(0) if WORKLOAD == "long_context_decode"
+     else W.qwen3_b64_decode(0, permute=False))
 kb, vb = bf16_bits(c.k_pool), bf16_bits(c.v_pool)
 tab, bi, ip, sl = (c.page_table.numpy(), c.batch_idx.numpy(), c.input_pos.numpy(),
                    c.seq_lens.numpy())
 kn, vn, q = bf16_bits(c.k_new), bf16_bits(c.v_new), bf16_bits(c.q)
 row_kv = [int(n) * c.num_kv_heads * c.head_dim * 4 for n in sl]
-res = {}
+res = {"host_cpu_count": os.cpu_count()}
 if MODE == "full":
-    # whole step: append of the 64 new tokens, then decode of all 64 rows
+    # whole step on one core: append of the new tokens, then decode of all rows
     times = []
     for _ in range(REPS):
         t0 = time.perf_counter()
         k2, v2, _ = orc.append(kb, vb, tab, kn, vn, bi, ip, c.page_size)
         orc.decode_attention(q, k2, v2, tab, bi, sl, c.page_size, c.scale)
         times.append(time.perf_counter() - t0)
-    res = {"seconds": statistics.median(times), "kv_bytes": sum(row_kv)}
+    res.update(seconds=statistics.median(times), kv_bytes=sum(row_kv), cores=1)
 else:
-    # one row per step (row i % 64), pools already holding the appended tokens
+    # decode rows spread over a pool of processes, one row per task; the
+    # pools already hold the appended tokens (the append is done once, untimed)
     k2, v2, _ = orc.append(kb, vb, tab, kn, vn, bi, ip, c.page_size)
-    tot_t, tot_b = 0.0, 0
-    for i in range(WARMUP + STEPS):
-        r = i % c.batch
-        t0 = time.perf_counter()
+
+    def one_row(r):
         orc.decode_attention(q, k2, v2, tab, bi, sl, c.page_size, c.scale, rows=[r])
-        dt = time.perf_counter() - t0
-        if i >= WARMUP:
-            tot_t += dt
-            tot_b += row_kv[r]
-    res = {"seconds": tot_t, "kv_bytes": tot_b, "steps": STEPS}
+        return None
+
+    # this process has never touched a GPU (CUDA_VISIBLE_DEVICES is empty):
+    # fork shares the pools with the workers without copying them
+    procs = NPROC or os.cpu_count() or 1
+    with mp.get_context("fork").Pool(procs) as pool:
+        pool.map(one_row, ROWS[:procs], chunksize=1)        # warm the workers
+        if MODE == "parallel":
+            times = []
+            for _ in range(REPS):
+                t0 = time.perf_counter()
+                pool.map(one_row, ROWS, chunksize=1)
+                times.append(time.perf_counter() - t0)
+            res.update(seconds=statistics.median(times),
+                       kv_bytes=sum(row_kv[r] for r in ROWS), cores=procs)
+        else:
+            # reference arm: STEPS timed steps after WARMUP, each the decode of
+            # PER_STEP rows (a block of rows, in turn)
+            tot_t, tot_b = 0.0, 0
+            for i in range(WARMUP + STEPS):
+                blk = [ROWS[(i * PER_STEP + j) % len(ROWS)] for j in range(PER_STEP)]
+                t0 = time.perf_counter()
+                pool.map(one_row, blk, chunksize=1)
+                dt = time.perf_counter() - t0
+                if i >= WARMUP:
+                    tot_t += dt
+                    tot_b += sum(row_kv[r] for r in blk)
+            res.update(seconds=tot_t, kv_bytes=tot_b, steps=STEPS, cores=procs)
 print(json.dumps(res))
 """
 
 
-def run_oracle_child(mode: str, reps: int = 5, steps: int = 0, warmup: int = 0):
-    """Runs the oracle, as it stands, in a child process with one BLAS thread
-    (started by subprocess, never forked from a process that touched CUDA)."""
-    code = (f"ROOT={ROOT!r}\nMODE={mode!r}\nREPS={reps}\nSTEPS={steps}\n"
-            f"WARMUP={warmup}\n") + _ORACLE_CHILD
+def run_oracle_child(mode: str, workload: str = "qwen3_b64_decode", reps: int = 5,
+                     rows=None, nproc: int = 0, steps: int = 0, warmup: int = 0,
+                     per_step: int = 0):
+    """Runs the oracle, as it stands, in a child process started by
+    subprocess (never forked from a process that touched CUDA) with one BLAS
+    thread per process. ``full``: the whole step on one core. ``parallel``:
+    decode of ``rows`` over a pool of ``nproc`` processes (0: all host
+    cores). ``steps``: the reference arm's timed steps."""
+    code = (f"ROOT={ROOT!r}\nMODE={mode!r}\nWORKLOAD={workload!r}\nREPS={reps}\n"
+            f"ROWS={list(rows or [])!r}\nNPROC={nproc}\nSTEPS={steps}\nWARMUP={warmup}\n"
+            f"PER_STEP={per_step}\n") + _ORACLE_CHILD
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1",
                MKL_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
@@ -219,19 +248,25 @@ def run_oracle_child(mode: str, reps: int = 5, steps: int = 0, warmup: int = 0):
 
 def run_reference(args):
     """Reference arm: the float64 CPU oracle on the same workload, metric and
-    unit; each step is a bounded sample (one of the 64 rows, in turn)."""
+    unit, on all host cores (one process per core, one row per task). Each
+    step decodes a block of rows of the 64 (all 64 when the run is short;
+    16 per step for runs of more than 1000 steps, so the default run stays
+    within minutes); the append is done once before timing."""
     world, rank, _ = _dist()
     if rank != 0:
         return
-    value, d = run_oracle_child("rows", steps=args.steps, warmup=args.warmup)
-    sample = "decode of one row per step (row = step mod 64), append done before timing"
+    per_step = 64 if args.steps + args.warmup <= 1000 else 16
+    value, d = run_oracle_child("steps", rows=list(range(64)), steps=args.steps,
+                                warmup=args.warmup, per_step=per_step)
+    sample = (f"decode of {per_step} of the 64 rows per step (blocks in turn), one row per "
+              f"task on {d['cores']} processes; append done once before timing")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": d["seconds"] / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "sample": sample},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": d["cores"], "kind": "oracle",
+                             "sample": sample, "host_cpu_count": d["host_cpu_count"]},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -269,11 +304,11 @@ def run_pkv(args):
     def kv_set_bytes(case):
         return 2 * case.k_pool.numel() * 2
 
-    def timed_decode(case, steps, warmup):
-        """Times `steps` decode steps (the fused append + decode call) replayed
-        from CUDA graphs, rotating over pool sets so each step's KV comes from
-        HBM; a second graph of decode calls alone gives the decode call's
-        duration, and a third the two-call step (append, then decode)."""
+    def decode_rig(case, warmup):
+        """Device copies of `case` (enough pool sets that each step's KV comes
+        from HBM), the call bodies (append, decode, fused step) on set i mod
+        n_sets, and a graph-capture helper; the calls are run eagerly first."""
+        import types
         n_sets = max(2, math.ceil(2 * L2_BYTES / kv_set_bytes(case)) + 1)
         sets = make_sets(case, n_sets)
         B, hq = case.batch, case.num_q_heads
@@ -302,14 +337,6 @@ def run_pkv(args):
                                                 case.scale, out=out, lse=lse, workspace=ws,
                                                 dev_err=err)
 
-        for i in range(max(warmup, n_sets)):   # eager warm-up (first-call set-up)
-            append(i)
-            decode(i)
-            fused(i)
-        torch.cuda.synchronize()
-
-        per_graph = n_sets * max(1, 96 // n_sets)
-
         def capture(n, body):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
@@ -317,13 +344,80 @@ def run_pkv(args):
                     body(i)
             return g
 
+        for i in range(max(warmup, n_sets)):   # eager warm-up (first-call set-up)
+            append(i)
+            decode(i)
+            fused(i)
+        torch.cuda.synchronize()
+        return types.SimpleNamespace(n_sets=n_sets, sets=sets, append=append, decode=decode,
+                                     fused=fused, capture=capture, err=err)
+
+    def check_err(err, what):
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(err.item()):#x} in {what}")
+
+    def replay_ms(g, n_calls, reps):
+        """Median per-call ms over `reps` timed replays of graph g (n_calls
+        calls each); the graph has been launched before."""
+        ms = []
+        for _ in range(reps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            ms.append(a.elapsed_time(b) / n_calls)
+        return ms
+
+    def timed_decode_config(case, reps=7):
+        """The fused step and the decode call alone on `case`, each from
+        replays of a graph of 48-odd calls over rotating pool sets (KV from
+        HBM); each graph is launched once untimed; medians of `reps`."""
+        rig = decode_rig(case, 3)
+        per_graph = rig.n_sets * max(1, 48 // rig.n_sets)
+        step_g = rig.capture(per_graph, rig.fused)
+        dec_g = rig.capture(per_graph, rig.decode)
+        step_g.replay()
+        dec_g.replay()
+        torch.cuda.synchronize()
+        step_ms = statistics.median(replay_ms(step_g, per_graph, reps))
+        dec_ms = statistics.median(replay_ms(dec_g, per_graph, reps))
+        check_err(rig.err, case.name)
+        del step_g, dec_g, rig
+        torch.cuda.empty_cache()
+        live = int((case.batch_idx != 0).sum())
+        db, sb = decode_bytes(case), step_bytes(case)
+        return {"workload": case.name, "batch": case.batch, "live_rows": live,
+                "kv_tokens": int(case.seq_lens[case.batch_idx != 0].long().sum()),
+                "step_us": step_ms * 1e3, "step_gbs": sb / (step_ms * 1e-3) / 1e9,
+                "decode_call_us": dec_ms * 1e3,
+                "decode_call_gbs": db / (dec_ms * 1e-3) / 1e9,
+                "frac_of_measured": db / (dec_ms * 1e-3) / 1e9 / hbm_peak,
+                "frac_of_nominal_8TBs": db / (dec_ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS,
+                "tokens_per_s_per_layer": live / (step_ms * 1e-3)}
+
+    def timed_decode(case, steps, warmup):
+        """Times `steps` decode steps (the fused append + decode call) replayed
+        from CUDA graphs, rotating over pool sets so each step's KV comes from
+        HBM; a second graph of decode calls alone gives the decode call's
+        duration, and a third the two-call step (append, then decode)."""
+        rig = decode_rig(case, warmup)
+        n_sets, append, decode, fused, capture, err = (rig.n_sets, rig.append, rig.decode,
+                                                       rig.fused, rig.capture, rig.err)
+
+        per_graph = n_sets * max(1, 96 // n_sets)
         step_g = capture(per_graph, fused)
         tail = steps % per_graph
         tail_g = capture(tail, fused) if tail else None
         dec_g = capture(per_graph, decode)
         two_g = capture(per_graph, lambda i: (append(i), decode(i)))
+        # every graph the timed region replays is launched untimed first, so
+        # no first launch of a freshly instantiated graph is timed
         for _ in range(max(1, warmup // per_graph)):
             step_g.replay()
+            if tail_g is not None:
+                tail_g.replay()
             dec_g.replay()
             two_g.replay()
         torch.cuda.synchronize()
@@ -348,16 +442,11 @@ def run_pkv(args):
         reps = max(3, min(50, steps // per_graph))
         dec_ms, two_ms = [], []
         for _ in range(reps):
-            for g, acc in ((dec_g, dec_ms), (two_g, two_ms)):
-                a = torch.cuda.Event(enable_timing=True)
-                b = torch.cuda.Event(enable_timing=True)
-                a.record()
-                g.replay()
-                b.record()
-                torch.cuda.synchronize()
-                acc.append(a.elapsed_time(b) / per_graph)
-        if int(err.item()) != 0:
-            raise RuntimeError(f"device error bits {int(err.item()):#x} during the bench")
+            dec_ms += replay_ms(dec_g, per_graph, 1)
+            two_ms += replay_ms(two_g, per_graph, 1)
+        check_err(err, "the decode step")
+        del step_g, tail_g, dec_g, two_g, rig
+        torch.cuda.empty_cache()
         dec_sorted = sorted(dec_ms)
         return dict(total_ms=total_ms, dec_ms=statistics.median(dec_ms),
                     two_call_ms=statistics.median(two_ms),
@@ -635,6 +724,11 @@ def run_pkv(args):
     perm256 = W.qwen3_b64_decode(0, permute=True, page_size=256)
     rp256 = timed_decode(perm256, max(args.steps // 4, 10), args.warmup)
     e2e_ms, h2d, d2h = e2e_decode(case, max(args.steps // 10, 10), args.warmup)
+    # the other decode workloads, and the batch sweep at the Qwen3-4B shape
+    configs = {"padded_bucket": timed_decode_config(W.padded_bucket_decode(0)),
+               "long_context_b256": timed_decode_config(W.long_context_decode(0))}
+    sweep = [timed_decode_config(W.qwen3_b64_decode(0, permute=False, batch=b))
+             for b in (8, 16, 32, 64, 128, 256)]
     prefill = timed_prefill(20)
     chunked = timed_chunked_prefill(20)
     mixed = timed_chunked_prefill(20, n_decode=48)
@@ -679,17 +773,38 @@ def run_pkv(args):
                 "ms_per_step": e2e_ms,
                 "transfers": "inputs: one pinned-host -> device copy; results: out and lse "
                              "written by the kernels into pinned host memory"},
+        "decode_configs": configs,
+        "batch_sweep": {"workload": "qwen3_b64_decode shape at batch B: Hq=32, Hkv=8, D=128, "
+                                    "page 128, keys U[512,1024], sequential pages, seed 0",
+                        "rows": sweep},
         "prefill": prefill,
         "chunked_prefill": chunked,
         "gpu_launches": 2 * args.steps,
         "clocks": r["clocks"],
     }
     if not args.no_cpu_baseline:
-        gbs, d = run_oracle_child("full", reps=5)
-        line["cpu_baseline"] = {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                "sample": "the full step (append 64 tokens + decode all 64 "
-                                          "rows), median of 5, one BLAS thread",
-                                "seconds_per_step": d["seconds"]}
+        # the oracle as it stands on the host cores: all 64 rows of the step
+        # over one process per core, then the whole step on one core, then a
+        # seeded sample of 64 of the 256 long-context rows over all cores
+        gbs, d = run_oracle_child("parallel", rows=list(range(64)), reps=5)
+        gbs1, d1 = run_oracle_child("full", reps=3)
+        long_rows = sorted(int(x) for x in
+                           torch.randperm(256, generator=torch.Generator().manual_seed(0))[:64])
+        gbsl, dl = run_oracle_child("parallel", workload="long_context_decode", rows=long_rows,
+                                    reps=3)
+        line["cpu_baseline"] = {
+            "value": gbs, "unit": UNIT, "cores": d["cores"], "kind": "oracle",
+            "sample": f"decode of all 64 rows of the step, one row per task on {d['cores']} "
+                      "processes (one BLAS thread each), append done once before timing; "
+                      "median of 5",
+            "host_cpu_count": d["host_cpu_count"], "seconds_per_step": d["seconds"],
+            "single_core": {"value": gbs1, "cores": 1, "seconds_per_step": d1["seconds"],
+                            "sample": "the full step (append 64 tokens + decode all 64 rows) "
+                                      "on one core, median of 3"},
+            "long_context_b256": {"value": gbsl, "cores": dl["cores"],
+                                  "seconds": dl["seconds"],
+                                  "sample": "decode of 64 seeded rows of the 256, one row per "
+                                            "task on all cores, median of 3"}}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

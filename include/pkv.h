@@ -230,7 +230,12 @@ pkv_status pkv_decode_append_attention(const pkv_cache_desc* cache, void* k_pool
  *    GQA group of 4 on a 152-SM GB300; use pkv_decode_attention beyond that).
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current and caches it; make that
- *    first call before any stream capture.
+ *    first call before any stream capture. A failed lookup returns
+ *    PKV_ERR_CUDA (its text in pkv_last_cuda_error_string()). The cached
+ *    address does not survive cudaDeviceReset: after a reset, do not use
+ *    this entry point on that device again in the same process.
+ *  - Other argument errors give the status pkv_decode_attention gives for
+ *    them (an empty batch is validated the same way and returns PKV_OK).
  *  - All calls share the one array. Its contents from the previous call are
  *    never read before being overwritten, so nothing needs clearing, but two
  *    calls whose kernels overlap on the GPU (different streams, or different

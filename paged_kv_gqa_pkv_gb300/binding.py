@@ -34,7 +34,8 @@ DEV_ERR_LAYOUT = 0x8
 DEV_ERR_TIMEOUT = 0x10
 
 EXPORTED = ("pkv_append", "pkv_append_rope", "pkv_decode_workspace_size", "pkv_decode_attention",
-            "pkv_decode_append_attention", "pkv_prefill_paged_attention",
+            "pkv_decode_append_attention", "pkv_decode_attention_static_scratch",
+            "pkv_prefill_paged_attention",
             "pkv_prefill_attention", "pkv_status_string",
             "pkv_status_from_device_error", "pkv_last_cuda_error_string")
 

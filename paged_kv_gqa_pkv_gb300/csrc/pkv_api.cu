@@ -46,16 +46,19 @@ pkv_status device_info(int* sm_count) {
   static DeviceInfo cache[kMaxDevices];
   static std::mutex mu;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return pkv::record_cuda_status(e);
   if (dev < 0 || dev >= kMaxDevices) return PKV_ERR_DEVICE;
   std::lock_guard<std::mutex> lock(mu);
   DeviceInfo& d = cache[dev];
   if (!d.known) {
     int major = 0, minor = 0, sms = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return PKV_ERR_CUDA;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) !=
+            cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) !=
+            cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return pkv::record_cuda_status(e);
     d.supported = (major == 10 && minor == 3);  // built for sm_103a only
     d.sm_count = sms;
     d.known = true;

@@ -13,10 +13,13 @@
 // The array's name in host code is only a host-side handle for the symbol, not
 // a device address: the device address is looked up with cudaGetSymbolAddress
 // the first time the entry point runs on a device (with that device current),
-// and cached per device.
+// and cached per device. The cache is not told about cudaDeviceReset: a
+// process that resets a device and keeps using this library on it holds a
+// stale address (the header says so).
 #include <mutex>
 
 #include "pkv.h"
+#include "pkv_launch.h"
 
 namespace {
 
@@ -54,13 +57,18 @@ extern "C" pkv_status pkv_decode_attention_static_scratch(
     const int32_t* page_table, const void* q, int num_q_heads, const int32_t* batch_idx,
     const int32_t* seq_lens, int batch, float scale, void* out, float* lse, int32_t* dev_err,
     cudaStream_t stream) {
-  if (batch == 0) return PKV_OK;
-  const size_t need = pkv_decode_workspace_size(cache, batch, num_q_heads, 0);
-  if (need == 0) return PKV_ERR_ARG;                  // invalid geometry or device
+  const size_t need =
+      batch > 0 ? pkv_decode_workspace_size(cache, batch, num_q_heads, 0) : size_t{0};
+  // An empty batch, or arguments the workspace entry point rejects (invalid
+  // descriptor, GQA group or batch, unsupported device): that entry point,
+  // given no workspace, runs the same checks and returns the same status.
+  if (need == 0)
+    return pkv_decode_attention(cache, k_pool, v_pool, page_table, q, num_q_heads, batch_idx,
+                                seq_lens, batch, scale, out, lse, nullptr, 0, dev_err, stream);
   if (need > kStaticScratchBytes) return PKV_ERR_WORKSPACE;  // past the fixed maximum
   cudaError_t err = cudaSuccess;
   void* scratch = scratch_address(&err);
-  if (scratch == nullptr) return PKV_ERR_CUDA;
+  if (scratch == nullptr) return pkv::record_cuda_status(err);
   return pkv_decode_attention(cache, k_pool, v_pool, page_table, q, num_q_heads, batch_idx,
                               seq_lens, batch, scale, out, lse, scratch, kStaticScratchBytes,
                               dev_err, stream);

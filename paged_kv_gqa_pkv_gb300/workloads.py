@@ -1,8 +1,10 @@
 """Seeded synthetic workloads for paged-KV GQA attention.
 
 This module only draws inputs: sequence lengths, page tables, pools and
-q/k/v. It holds none of the attention arithmetic and none of the addressing
-that the kernels or the oracle perform, so both sides can use it.
+q/k/v. It holds none of the attention arithmetic, so both sides can use it.
+One address computation appears here, in ``chunked_prefill``: to place real
+prefix data in a pool otherwise filled with a marker value it maps each
+prefix token to its pool row. Neither the kernels nor the oracle use it.
 
 The shapes follow the Qwen3-4B attention layer the source pages benchmark
 (32 query heads, 8 KV heads, head dim 128; "qwen3_flex_inference.py",

@@ -1,8 +1,8 @@
 """Chunked prefill over the paged cache (``pkv_prefill_paged_attention``) on
 the GPU against the oracle's ``paged_prefill_attention``: the chunks' K/V are
 appended first (``pkv_append``), then every packed token attends its slot's
-keys 0..input_pos through the pages. Full-size cases compare sampled tokens
-(the oracle is a per-token loop); small cases compare every token."""
+keys 0..input_pos through the pages. Every token is compared: the full-size
+step runs the oracle over all host cores."""
 
 import numpy as np
 import pytest
@@ -12,6 +12,7 @@ import oracle.paged_attention as orc
 from paged_kv_gqa_pkv_gb300 import binding
 from paged_kv_gqa_pkv_gb300 import workloads as W
 from paged_kv_gqa_pkv_gb300.workloads import bf16_bits
+from tests import oracle_pool
 from tests.parity import assert_attention_close, gpu, new_dev_err
 
 pytestmark = pytest.mark.gpu
@@ -43,29 +44,23 @@ def oracle_chunked(c, rows=None, table=None):
     return out, lse, bad_tok, bad
 
 
-def _sample_rows(c, n=240, seed=0):
-    """Every chunk's first and last token, every decode token, plus random
-    tokens."""
-    b = c.batch_idx.numpy()
-    picks = set()
-    for i in range(len(b)):
-        if i == 0 or b[i] != b[i - 1] or i == len(b) - 1 or b[i + 1] != b[i]:
-            picks.add(i)
-    rng = np.random.default_rng(seed)
-    picks.update(rng.choice(len(b), size=min(n, len(b)), replace=False).tolist())
-    return sorted(picks)
-
-
-def test_mixed_chunked_step_full_size_sampled():
+def test_mixed_chunked_step_full_size_every_row():
     """16 chunks of 512 tokens over prefixes U[512, 4096] plus 48 decode
-    tokens, shuffled (the default chunked workload, page 128)."""
+    tokens, shuffled (the default chunked workload, page 128): every token of
+    every head against the oracle, run over all host cores."""
     c = W.chunked_prefill(0)
-    _, _, out, lse, err = run_chunked(c)
-    rows = _sample_rows(c)
-    ref_o, ref_l, bad_tok, bad = oracle_chunked(c, rows=rows)
-    assert err == 0 and not bad_tok and not bad
-    assert_attention_close(out, lse, ref_o, ref_l, rows=rows, tag="chunked full")
-    assert not torch.isnan(out.float()).any()
+    kp, vp, out, lse, err = run_chunked(c)
+    t = c.page_table.numpy()
+    kb, vb, bad_tok = orc.append(bf16_bits(c.k_pool), bf16_bits(c.v_pool), t, bf16_bits(c.k_new),
+                                 bf16_bits(c.v_new), c.batch_idx.numpy(), c.input_pos.numpy(),
+                                 c.page_size)
+    assert err == 0 and not bad_tok
+    assert np.array_equal(bf16_bits(kp), kb) and np.array_equal(bf16_bits(vp), vb)
+    ro_bits, rl, bad = oracle_pool.paged_prefill_all_rows(
+        bf16_bits(c.q), kb, vb, t, c.batch_idx.numpy(), c.input_pos.numpy(), c.page_size,
+        c.scale)
+    assert not bad and not np.isnan(rl).any()
+    assert_attention_close(out, lse, orc.bf16_bits_to_f64(ro_bits), rl, tag="chunked full")
 
 
 @pytest.mark.parametrize("ps", [16, 32, 64, 128, 256])

@@ -5,9 +5,11 @@ start-up, or plug-in hosts that forbid allocations while running cannot pass
 ``pkv_decode_attention`` a workspace. ``pkv_decode_attention_static_scratch``
 serves them from a scratch array built into the library. Here it is called
 through the C ABI twice in a row and must agree with the workspace entry
-point on the same inputs, within the attention tolerance used throughout the
-tests. This file is collected last so that a stop-at-first-failure run has
-already run every other test.
+point on the same inputs, and with the oracle, within the attention
+tolerance used throughout the tests; once its first call on the device has
+run, further calls must leave the device's free memory unchanged. This file
+is collected last so that a stop-at-first-failure run has already run every
+other test.
 """
 
 import pytest
@@ -15,7 +17,8 @@ import torch
 
 from paged_kv_gqa_pkv_gb300 import binding
 from paged_kv_gqa_pkv_gb300 import workloads as W
-from tests.parity import OUT_MAX_ABS, OUT_MEAN_ABS, LSE_ABS, gpu, new_dev_err
+from tests.parity import (OUT_MAX_ABS, OUT_MEAN_ABS, LSE_ABS, assert_attention_close, gpu,
+                          new_dev_err, oracle_decode_step)
 
 pytestmark = pytest.mark.gpu
 
@@ -62,3 +65,53 @@ def test_static_scratch_rejects_batches_past_its_limit():
         binding.pkv_decode_attention_static_scratch(
             x["k_pool"], x["v_pool"], x["page_table"], q, z, z, case.page_size, case.scale)
     assert e.value.status == 4
+
+
+def test_static_scratch_matches_oracle_and_allocates_nothing():
+    case = W.tiny_decode(0)
+    x = _inputs(case)
+    # attend the pools as they stand (no append), against the oracle on the same pools
+    _, _, ref_o, ref_l, _, bad_rows = oracle_decode_step(case, append=False)
+    assert not bad_rows
+    B, hq = case.q.shape[0], case.num_q_heads
+    out = torch.empty((B, hq, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, hq), dtype=torch.float32, device="cuda")
+    err = new_dev_err()
+
+    def call():
+        binding.pkv_decode_attention_static_scratch(
+            x["k_pool"], x["v_pool"], x["page_table"], x["q"], x["batch_idx"], x["seq_lens"],
+            case.page_size, case.scale, out=out, lse=lse, dev_err=err)
+
+    call()                      # the first call on a device may load the library's module
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    used0 = torch.cuda.memory_allocated()
+    for _ in range(2):
+        out.fill_(float("nan"))
+        call()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert_attention_close(out.cpu(), lse.cpu(), ref_o, ref_l, tag="static scratch")
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0 and torch.cuda.memory_allocated() == used0
+
+
+def test_static_scratch_empty_batch_and_bad_arguments_match_workspace_entry_point():
+    case = W.tiny_decode(0)
+    x = _inputs(case)
+    q0 = torch.zeros((0, case.num_q_heads, 128), dtype=torch.bfloat16, device="cuda")
+    z0 = torch.zeros(0, dtype=torch.int32, device="cuda")
+    out, lse = binding.pkv_decode_attention_static_scratch(
+        x["k_pool"], x["v_pool"], x["page_table"], q0, z0, z0, case.page_size, case.scale)
+    assert out.shape[0] == 0 and lse.shape[0] == 0
+    # a GQA group the kernels do not serve (3 q heads per kv head): both entry points say ARG
+    q3 = torch.zeros((2, 3 * case.num_kv_heads, 128), dtype=torch.bfloat16, device="cuda")
+    z2 = torch.ones(2, dtype=torch.int32, device="cuda")
+    for fn in (binding.pkv_decode_attention_static_scratch, binding.pkv_decode_attention):
+        with pytest.raises(binding.PkvError) as e:
+            kw = {} if fn is binding.pkv_decode_attention_static_scratch else {
+                "workspace": torch.empty(1 << 20, dtype=torch.uint8, device="cuda")}
+            fn(x["k_pool"], x["v_pool"], x["page_table"], q3, z2, z2, case.page_size,
+               case.scale, **kw)
+        assert e.value.status == 1
