@@ -596,6 +596,7 @@ def run_pkv(args):
                 "append_gbs": (c.n_tokens * c.num_kv_heads * c.head_dim * 2 * 4)
                 / (app_us * 1e-6) / 1e9,
                 "append_rope_knorm_call_us": rope_us,
+                "append_rope_knorm_traffic": captured_traffic("append_rope_call"),
                 "append_rope_knorm_gbs": (c.n_tokens * c.num_kv_heads * c.head_dim * 2 * 4)
                 / (rope_us * 1e-6) / 1e9}
 
