@@ -19,9 +19,9 @@
 //    into a 3-slot ring of 32 KB half-stages, in the MMA thread's order
 //    (K_0, then K_j+1 and V_j for each j, continuing across items), starting
 //    at the first key any row of the tile can see;
-//  * warp 1 (one thread) issues tcgen05 MMAs: S_h = Q_h K^T into TMEM and
-//    O_h += P_h V. The next tile's S_h is computed as soon as the softmax has
-//    read the current S_h into registers (s_free), so QK of tile j+1 runs
+//  * warp 1 issues tcgen05 MMAs (one elected lane): S_h = Q_h K^T into TMEM
+//    and O_h += P_h V. The next tile's S_h is computed as soon as the softmax
+//    has read the current S_h into registers (s_free), so QK of tile j+1 runs
 //    while the softmax of tile j computes its exponentials;
 //  * warps 2..5 and 6..9 are the softmax warpgroups of the two heads, one
 //    query row per thread (its TMEM lane): masked online softmax in fp32 with
@@ -250,35 +250,64 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
     }
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer ----
-    uint32_t C = 0;       // ring slots consumed
-    uint32_t qi = 0;      // non-empty items
-    uint32_t tc = 0;      // KV tiles processed (all items)
-    const uint32_t sQ = smem_u32(smem + kOffQ);
-    const uint32_t sP = smem_u32(smem + kOffP);
+    // The whole warp runs this loop, so its bookkeeping stays warp-uniform,
+    // and one elected lane issues the tensor instructions. Per tile the MMAs
+    // go out in two bursts, QK of both heads and PV of both heads, each after
+    // one round of waits and with every descriptor word computed before it:
+    // the tensor pipe accepts one MMA at a time, so anything issued between
+    // two MMAs (the warp shares its SM sub-partition with busy softmax warps)
+    // leaves the pipe idle.
+    uint32_t slot = 0, phase = 0;  // ring slot and parity of the next tile consumed
+    uint32_t qi = 0;               // non-empty items
+    uint32_t tc = 0;               // KV tiles processed (all items)
     const uint32_t sR = smem_u32(smem + kOffRing);
-    auto qk = [&](int h, uint32_t kslot) {
-      const uint32_t q = sQ + h * kTileBytes;
-      const uint32_t k = sR + kslot * kTileBytes;
-      const uint32_t d = tmem + static_cast<uint32_t>(h * kBN);  // S_h
-#pragma unroll
-      for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-        umma_bf16(d, sw128_desc(q + off, 0, 1024), sw128_desc(k + off, 0, 1024), kIdescQK,
-                  kk > 0 ? 1u : 0u);
-      }
-      umma_commit(&s_full[h]);
+    const bool two = hpi == 2;
+    uint32_t qd[2][8], pd[2][8];
+    kmajor_steps(smem_u32(smem + kOffQ), qd[0]);
+    kmajor_steps(smem_u32(smem + kOffQ + kTileBytes), qd[1]);
+    kmajor_steps(smem_u32(smem + kOffP), pd[0]);
+    kmajor_steps(smem_u32(smem + kOffP + kTileBytes), pd[1]);
+    // every lane tests the barrier; lane 0's outcome is the warp's
+    auto wait_w = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __shfl_sync(0xffffffffu, wait_or_abort(bar, parity, s_abort) ? 1 : 0, 0) != 0;
     };
-    auto pv = [&](int h, uint32_t vslot, bool accumulate) {
-      const uint32_t pp = sP + h * kTileBytes;
-      const uint32_t v = sR + vslot * kTileBytes;
-      const uint32_t d = tmem + static_cast<uint32_t>(256 + h * kHeadDim);  // O_h
-#pragma unroll
-      for (int kk = 0; kk < kBN / 16; ++kk) {
-        const uint32_t a_off = (kk >> 2) * kHalf + (kk & 3) * 32;
-        umma_bf16(d, sw128_desc(pp + a_off, 0, 1024), sw128_desc(v + kk * 2048, kHalf, 1024),
-                  kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+    auto wait_heads = [&](uint64_t* bar2, uint32_t parity) -> bool {
+      return wait_w(&bar2[0], parity) && (!two || wait_w(&bar2[1], parity));
+    };
+    auto next_slot = [&]() {
+      if (++slot == kRing) {
+        slot = 0;
+        phase ^= 1u;
       }
-      umma_commit(&pv_done[h]);
+    };
+    auto issue_qk = [&](uint32_t kslot, bool last_k) {  // S_h = Q_h K^T, both heads
+      uint32_t kb[8];
+      kmajor_steps(sR + kslot * kTileBytes, kb);
+      if (elect_one()) {
+        umma8_ss(tmem, qd[0], kb, kIdescQK, 0u);
+        umma_commit(&s_full[0]);
+        if (two) {
+          umma8_ss(tmem + kBN, qd[1], kb, kIdescQK, 0u);
+          umma_commit(&s_full[1]);
+        }
+        umma_commit(&ring_empty[kslot]);
+        if (last_k) umma_commit(q_empty);  // the item's Q is read for good
+      }
+      __syncwarp();
+    };
+    auto issue_pv = [&](uint32_t vslot, uint32_t acc) {  // O_h (+)= P_h V, both heads
+      uint32_t vb[8];
+      vmn_steps(sR + vslot * kTileBytes, vb);
+      if (elect_one()) {
+        umma8_ss(tmem + 256, pd[0], vb, kIdescPV, acc);
+        umma_commit(&pv_done[0]);
+        if (two) {
+          umma8_ss(tmem + 256 + kHeadDim, pd[1], vb, kIdescPV, acc);
+          umma_commit(&pv_done[1]);
+        }
+        umma_commit(&ring_empty[vslot]);
+      }
+      __syncwarp();
     };
     TileRaw raw = tile_raw_load(p, item_r0(p, blockIdx.x, items_per_tile), lane);
     for (int item = blockIdx.x; item < p.n_items && !*s_abort; item += gridDim.x) {
@@ -288,55 +317,39 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
       raw = tile_raw_load(p, item_r0(p, item + gridDim.x, items_per_tile), lane);
       if (kv_hi <= kv_lo) continue;
       const int n_kv = (kv_hi - kv_lo + kBN - 1) / kBN;
-      if (lane == 0) {
-        // QK of one tile for every head of the item; S_h must have been read
-        // by the softmax of the previous tile (global tile count t)
-        auto qk_all = [&](uint32_t kslot, uint32_t t) -> bool {
-          for (int h = 0; h < hpi; ++h) {
-            if (t > 0 && !wait_or_abort(&s_free[h], (t - 1) & 1, s_abort)) return false;
-            tc_fence_after();
-            qk(h, kslot);
-          }
-          umma_commit(&ring_empty[kslot]);
-          return true;
-        };
-        bool ok = wait_or_abort(q_full, qi & 1, s_abort);
-        uint32_t kslot = C % kRing;
-        ok = ok && wait_or_abort(&ring_full[kslot], (C / kRing) & 1, s_abort);
-        ++C;
-        if (ok) {
-          tc_fence_after();
-          ok = qk_all(kslot, tc);
-          if (ok && n_kv == 1) umma_commit(q_empty);
-        }
-        for (int j = 0; ok && j < n_kv; ++j) {
-          if (j + 1 < n_kv) {
-            // K_{j+1}: S of the next tile while this tile's softmax runs
-            kslot = C % kRing;
-            if (!wait_or_abort(&ring_full[kslot], (C / kRing) & 1, s_abort)) { ok = false; break; }
-            ++C;
-            if (!qk_all(kslot, tc + 1)) { ok = false; break; }
-            if (j + 2 == n_kv) umma_commit(q_empty);
-          }
-          const uint32_t vslot = C % kRing;
-          if (!wait_or_abort(&ring_full[vslot], (C / kRing) & 1, s_abort)) { ok = false; break; }
-          ++C;
-          for (int h = 0; h < hpi && ok; ++h) {
-            if (!wait_or_abort(&p_full[h], tc & 1, s_abort)) { ok = false; break; }
-            if (j == 0 && qi > 0 && !wait_or_abort(&o_free[h], (qi - 1) & 1, s_abort)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            pv(h, vslot, j > 0);
-          }
-          if (!ok) break;
-          umma_commit(&ring_empty[vslot]);
-          ++tc;
-        }
-        if (!ok) *s_abort = 1;
+      // K_0: S_h must have been read by the softmax of the previous tile
+      bool ok = wait_w(q_full, qi & 1);
+      uint32_t kslot = slot;
+      ok = ok && wait_w(&ring_full[kslot], phase);
+      next_slot();
+      if (ok && tc > 0) ok = wait_heads(s_free, (tc - 1) & 1);
+      if (ok) {
+        tc_fence_after();
+        issue_qk(kslot, n_kv == 1);
       }
-      __syncwarp();
+      for (int j = 0; ok && j < n_kv; ++j) {
+        if (j + 1 < n_kv) {
+          // K_{j+1}: S of the next tile while this tile's softmax runs
+          kslot = slot;
+          ok = wait_w(&ring_full[kslot], phase);
+          next_slot();
+          ok = ok && wait_heads(s_free, tc & 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_qk(kslot, j + 2 == n_kv);
+        }
+        const uint32_t vslot = slot;
+        ok = wait_w(&ring_full[vslot], phase);
+        next_slot();
+        ok = ok && wait_heads(p_full, tc & 1);
+        // the first PV of an item overwrites O_h: its previous epilogue is done
+        if (ok && j == 0 && qi > 0) ok = wait_heads(o_free, (qi - 1) & 1);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(vslot, j > 0 ? 1u : 0u);
+        ++tc;
+      }
+      if (!ok) *s_abort = 1;
       ++qi;
     }
   } else {

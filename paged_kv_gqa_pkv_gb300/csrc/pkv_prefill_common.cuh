@@ -40,6 +40,97 @@ __device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, u
       : "memory");
 }
 
+// Shared-memory descriptors (tcgen05 format, as sw128_desc) split in 32-bit
+// words. Every operand here has 8-row groups 1024 bytes apart and 128-byte
+// swizzle, so the high word is one constant; the low word holds the start
+// address (>> 4) and the leading byte offset.
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+
+// The eight K-steps of one 128 x 128 x 128 product, D (+)= sum_k A_k B_k, as
+// eight tcgen05.mma from one asm block with nothing issued between them. The
+// issuing warp shares its SM sub-partition with busy softmax warps; with the
+// descriptor arithmetic done before the block, each MMA needs one issue slot
+// and the tensor pipe is fed close to its rate (issued one by one with the
+// arithmetic in between, a 128 x 128 x 16 MMA took ~150 cycles to issue
+// against the 64 it executes in). a_lo/b_lo: low descriptor words per K-step
+// (shared-memory A and B); the first MMA accumulates iff `accumulate`.
+__device__ __forceinline__ void umma8_ss(uint32_t d, const uint32_t (&a_lo)[8],
+                                         const uint32_t (&b_lo)[8], uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 a<8>, b<8>;\n\t"
+      "setp.ne.b32 p0, %17, 0;\n\tsetp.eq.b32 p1, %17, %17;\n\t"
+      "mov.b64 a0, {%1, %19};\n\tmov.b64 b0, {%9, %19};\n\t"
+      "mov.b64 a1, {%2, %19};\n\tmov.b64 b1, {%10, %19};\n\t"
+      "mov.b64 a2, {%3, %19};\n\tmov.b64 b2, {%11, %19};\n\t"
+      "mov.b64 a3, {%4, %19};\n\tmov.b64 b3, {%12, %19};\n\t"
+      "mov.b64 a4, {%5, %19};\n\tmov.b64 b4, {%13, %19};\n\t"
+      "mov.b64 a5, {%6, %19};\n\tmov.b64 b5, {%14, %19};\n\t"
+      "mov.b64 a6, {%7, %19};\n\tmov.b64 b6, {%15, %19};\n\t"
+      "mov.b64 a7, {%8, %19};\n\tmov.b64 b7, {%16, %19};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a0, b0, %18, p0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %18, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %18, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %18, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a4, b4, %18, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a5, b5, %18, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a6, b6, %18, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a7, b7, %18, p1;\n\t}" ::"r"(d),
+      "r"(a_lo[0]), "r"(a_lo[1]), "r"(a_lo[2]), "r"(a_lo[3]), "r"(a_lo[4]), "r"(a_lo[5]),
+      "r"(a_lo[6]), "r"(a_lo[7]), "r"(b_lo[0]), "r"(b_lo[1]), "r"(b_lo[2]), "r"(b_lo[3]),
+      "r"(b_lo[4]), "r"(b_lo[5]), "r"(b_lo[6]), "r"(b_lo[7]), "r"(accumulate), "r"(idesc),
+      "n"(kDescHi)
+      : "memory");
+}
+
+// The same with A read from tensor memory: K-step k takes its A operand at
+// TMEM address a_tmem + 8k (bf16 pairs, 16 keys per 8 columns).
+__device__ __forceinline__ void umma8_ts(uint32_t d, uint32_t a_tmem, const uint32_t (&b_lo)[8],
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 b<8>;\n\t.reg .b32 t<8>;\n\t"
+      "setp.ne.b32 p0, %10, 0;\n\tsetp.eq.b32 p1, %10, %10;\n\t"
+      "mov.b64 b0, {%2, %12};\n\tadd.u32 t0, %1, 0;\n\t"
+      "mov.b64 b1, {%3, %12};\n\tadd.u32 t1, %1, 8;\n\t"
+      "mov.b64 b2, {%4, %12};\n\tadd.u32 t2, %1, 16;\n\t"
+      "mov.b64 b3, {%5, %12};\n\tadd.u32 t3, %1, 24;\n\t"
+      "mov.b64 b4, {%6, %12};\n\tadd.u32 t4, %1, 32;\n\t"
+      "mov.b64 b5, {%7, %12};\n\tadd.u32 t5, %1, 40;\n\t"
+      "mov.b64 b6, {%8, %12};\n\tadd.u32 t6, %1, 48;\n\t"
+      "mov.b64 b7, {%9, %12};\n\tadd.u32 t7, %1, 56;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t0], b0, %11, p0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t1], b1, %11, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t2], b2, %11, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t3], b3, %11, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t4], b4, %11, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t5], b5, %11, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t6], b6, %11, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [t7], b7, %11, p1;\n\t}" ::"r"(d),
+      "r"(a_tmem), "r"(b_lo[0]), "r"(b_lo[1]), "r"(b_lo[2]), "r"(b_lo[3]), "r"(b_lo[4]),
+      "r"(b_lo[5]), "r"(b_lo[6]), "r"(b_lo[7]), "r"(accumulate), "r"(idesc), "n"(kDescHi)
+      : "memory");
+}
+
+// Low descriptor words of the eight K-steps of a K-major 128 x 128 tile at
+// `base` (two 16 KB halves of 64 elements; K-step k at half k / 4, 32 bytes
+// per step within it).
+__device__ __forceinline__ void kmajor_steps(uint32_t base, uint32_t (&lo)[8]) {
+  const uint32_t b = desc_lo(base, 0);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) lo[kk] = b + ((((kk >> 2) * kHalf) + (kk & 3) * 32) >> 4);
+}
+
+// ... of an MN-major V tile at `base` used as the B operand of PV: K-step k
+// (16 keys) starts 2 KB in; the two 64-dim halves are kHalf apart (LBO).
+__device__ __forceinline__ void vmn_steps(uint32_t base, uint32_t (&lo)[8]) {
+  const uint32_t b = desc_lo(base, kHalf);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) lo[kk] = b + ((kk * 2048) >> 4);
+}
+
 // 16 consecutive 32-bit columns of this thread's TMEM lane (warp-collective).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(

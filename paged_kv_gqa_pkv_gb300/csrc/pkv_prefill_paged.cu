@@ -368,25 +368,18 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
     const uint32_t sQ = smem_u32(smem + kOffQ);
     const uint32_t sR = smem_u32(smem + kOffRing);
     auto qk = [&](int h, uint32_t kslot) {
-      const uint32_t q = sQ + h * kTileBytes;
-      const uint32_t k = sR + kslot * kTileBytes;
-      const uint32_t d = tmem + static_cast<uint32_t>(h * kBN);  // S_h
-#pragma unroll
-      for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-        umma_bf16(d, sw128_desc(q + off, 0, 1024), sw128_desc(k + off, 0, 1024), kIdescQK,
-                  kk > 0 ? 1u : 0u);
-      }
+      uint32_t a[8], b[8];
+      kmajor_steps(sQ + h * kTileBytes, a);
+      kmajor_steps(sR + kslot * kTileBytes, b);
+      umma8_ss(tmem + static_cast<uint32_t>(h * kBN), a, b, kIdescQK, 0u);  // S_h
       umma_commit(&s_full[h]);
     };
     auto pv = [&](int h, uint32_t vslot, bool accumulate) {
-      const uint32_t a = tmem + static_cast<uint32_t>(h * kBN);             // P_h, over S_h
-      const uint32_t v = sR + vslot * kTileBytes;
-      const uint32_t d = tmem + static_cast<uint32_t>(256 + h * kHeadDim);  // O_h
-#pragma unroll
-      for (int kk = 0; kk < kBN / 16; ++kk)
-        umma_bf16_ts(d, a + kk * 8, sw128_desc(v + kk * 2048, kHalf, 1024), kIdescPV,
-                     (accumulate || kk > 0) ? 1u : 0u);
+      uint32_t b[8];
+      vmn_steps(sR + vslot * kTileBytes, b);
+      umma8_ts(tmem + static_cast<uint32_t>(256 + h * kHeadDim),          // O_h
+               tmem + static_cast<uint32_t>(h * kBN), b, kIdescPV,        // P_h, over S_h
+               accumulate ? 1u : 0u);
       umma_commit(&pv_done[h]);
     };
     TileRows nxt = tile_rows_load(p, item_r0(p, blockIdx.x, items_per_tile), lane);
