@@ -246,7 +246,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool b_mn_ma
          | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
-// True in exactly one active lane of the (converged) warp.
+// True in one lane of the converged warp: the lowest active lane, the same
+// one at every call with the same active lanes, so MMAs issued and committed
+// under it all come from one thread.
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred = 0;
   asm volatile(

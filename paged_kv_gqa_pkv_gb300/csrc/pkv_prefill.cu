@@ -251,12 +251,13 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer ----
     // The whole warp runs this loop, so its bookkeeping stays warp-uniform,
-    // and one elected lane issues the tensor instructions. Per tile the MMAs
-    // go out in two bursts, QK of both heads and PV of both heads, each after
-    // one round of waits and with every descriptor word computed before it:
-    // the tensor pipe accepts one MMA at a time, so anything issued between
-    // two MMAs (the warp shares its SM sub-partition with busy softmax warps)
-    // leaves the pipe idle.
+    // and one elected lane issues every tensor instruction (always the same
+    // lane: a commit tracks only the MMAs of the thread that commits). Per tile the MMAs go out in two
+    // bursts, QK of both heads and PV of both heads, each after one round of
+    // waits and with every descriptor word computed before it: the tensor
+    // pipe accepts one MMA at a time, so anything issued between two MMAs
+    // (the warp shares its SM sub-partition with busy softmax warps) leaves
+    // the pipe idle.
     uint32_t slot = 0, phase = 0;  // ring slot and parity of the next tile consumed
     uint32_t qi = 0;               // non-empty items
     uint32_t tc = 0;               // KV tiles processed (all items)

@@ -362,25 +362,42 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
     }
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer ----
+    // The whole warp runs this loop (warp-uniform bookkeeping; all lanes zero
+    // stale V rows) and one elected lane issues every tensor instruction
+    // (always the same lane: a commit tracks only the MMAs of the thread that
+    // commits), with every descriptor word computed before each burst:
+    // anything issued between two MMAs leaves the tensor pipe idle. Per tile
+    // and head: PV_h, then the head's next QK once that PV has read P_h (P_h
+    // sits on S_h). (PV of both heads first, then the QKs, measured slower.)
     uint32_t C = 0;       // ring slots consumed
     uint32_t qi = 0;      // non-empty items
     uint32_t tc = 0;      // KV tiles processed (all items)
-    const uint32_t sQ = smem_u32(smem + kOffQ);
     const uint32_t sR = smem_u32(smem + kOffRing);
-    auto qk = [&](int h, uint32_t kslot) {
-      uint32_t a[8], b[8];
-      kmajor_steps(sQ + h * kTileBytes, a);
-      kmajor_steps(sR + kslot * kTileBytes, b);
-      umma8_ss(tmem + static_cast<uint32_t>(h * kBN), a, b, kIdescQK, 0u);  // S_h
-      umma_commit(&s_full[h]);
+    uint32_t qd[2][8];
+    kmajor_steps(smem_u32(smem + kOffQ), qd[0]);
+    kmajor_steps(smem_u32(smem + kOffQ + kTileBytes), qd[1]);
+    // every lane tests the barrier; lane 0's outcome is the warp's
+    auto wait_w = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __shfl_sync(0xffffffffu, wait_or_abort(bar, parity, s_abort) ? 1 : 0, 0) != 0;
     };
-    auto pv = [&](int h, uint32_t vslot, bool accumulate) {
-      uint32_t b[8];
-      vmn_steps(sR + vslot * kTileBytes, b);
-      umma8_ts(tmem + static_cast<uint32_t>(256 + h * kHeadDim),          // O_h
-               tmem + static_cast<uint32_t>(h * kBN), b, kIdescPV,        // P_h, over S_h
-               accumulate ? 1u : 0u);
-      umma_commit(&pv_done[h]);
+    auto issue_qk = [&](int h, const uint32_t (&kb)[8]) {  // S_h = Q_h K^T
+      if (elect_one()) {
+        umma8_ss(tmem + static_cast<uint32_t>(h * kBN), qd[h], kb, kIdescQK, 0u);
+        umma_commit(&s_full[h]);
+      }
+      __syncwarp();
+    };
+    auto issue_pv = [&](int h, const uint32_t (&vb)[8], uint32_t acc) {  // O_h (+)= P_h V
+      if (elect_one()) {
+        umma8_ts(tmem + static_cast<uint32_t>(256 + h * kHeadDim),  // O_h
+                 tmem + static_cast<uint32_t>(h * kBN), vb, kIdescPV, acc);  // P_h, over S_h
+        umma_commit(&pv_done[h]);
+      }
+      __syncwarp();
+    };
+    auto commit_w = [&](uint64_t* bar) {
+      if (elect_one()) umma_commit(bar);
+      __syncwarp();
     };
     TileRows nxt = tile_rows_load(p, item_r0(p, blockIdx.x, items_per_tile), lane);
     for (int item = blockIdx.x; item < p.n_items && !*s_abort; item += gridDim.x) {
@@ -391,27 +408,24 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
       if (n_kv == 0) continue;
       RunCursor vc;
       cursor_first(vc, cur, rm, lane);
-      bool ok = true;
       const uint32_t k0slot = C % kRing;
-      if (lane == 0) {
-        ok = wait_or_abort(q_full, qi & 1, s_abort) &&
-             wait_or_abort(&ring_full[k0slot], (C / kRing) & 1, s_abort);
+      bool ok = wait_w(q_full, qi & 1) && wait_w(&ring_full[k0slot], (C / kRing) & 1);
+      if (ok) {
+        uint32_t kb[8];
+        kmajor_steps(sR + k0slot * kTileBytes, kb);
         // S_h is free once the previous item's last PV_h has read P_h from it
         for (int h = 0; ok && h < hpi; ++h) {
-          if (tc > 0 && !wait_or_abort(&pv_done[h], (tc - 1) & 1, s_abort)) {
-            ok = false;
-            break;
-          }
+          if (tc > 0) ok = wait_w(&pv_done[h], (tc - 1) & 1);
+          if (!ok) break;
           tc_fence_after();
-          qk(h, k0slot);
+          issue_qk(h, kb);
         }
         if (ok) {
-          umma_commit(&ring_empty[k0slot]);
-          if (n_kv == 1) umma_commit(q_empty);
+          commit_w(&ring_empty[k0slot]);
+          if (n_kv == 1) commit_w(q_empty);
         }
       }
       ++C;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
       for (int t = 0; ok && t < n_kv; ++t) {
         // ring order: K_{t+1} (if any), then V_t
         const bool more = t + 1 < n_kv;
@@ -439,38 +453,29 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
           fence_proxy_async_smem();
         }
         __syncwarp();
-        if (lane == 0) {
-          if (more && !wait_or_abort(&ring_full[kslot], (ck / kRing) & 1, s_abort)) ok = false;
-          for (int h = 0; h < hpi && ok; ++h) {
-            if (!wait_or_abort(&p_full[h], tc & 1, s_abort)) {
-              ok = false;
-              break;
-            }
-            if (t == 0 && qi > 0 && !wait_or_abort(&o_free[h], (qi - 1) & 1, s_abort)) {
-              ok = false;
-              break;
-            }
+        uint32_t vb[8], kb[8];
+        vmn_steps(sR + vslot * kTileBytes, vb);
+        kmajor_steps(sR + kslot * kTileBytes, kb);
+        if (more) ok = wait_w(&ring_full[kslot], (ck / kRing) & 1);
+        for (int h = 0; h < hpi && ok; ++h) {
+          ok = wait_w(&p_full[h], tc & 1);
+          if (ok && t == 0 && qi > 0) ok = wait_w(&o_free[h], (qi - 1) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(h, vb, t > 0 ? 1u : 0u);
+          if (more) {
+            ok = wait_w(&pv_done[h], tc & 1);
+            if (!ok) break;
             tc_fence_after();
-            pv(h, vslot, t > 0);
-            if (more) {
-              // the next S_h overwrites P_h: wait until this PV has read it
-              if (!wait_or_abort(&pv_done[h], tc & 1, s_abort)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              qk(h, kslot);
-            }
-          }
-          if (ok) {
-            umma_commit(&ring_empty[vslot]);
-            if (more) {
-              umma_commit(&ring_empty[kslot]);
-              if (t + 2 == n_kv) umma_commit(q_empty);
-            }
+            issue_qk(h, kb);
           }
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        commit_w(&ring_empty[vslot]);
+        if (more) {
+          commit_w(&ring_empty[kslot]);
+          if (t + 2 == n_kv) commit_w(q_empty);
+        }
         ++tc;
         cursor_next(vc, cur, rm, lane);
       }
