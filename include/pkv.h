@@ -309,6 +309,27 @@ pkv_status pkv_prefill_attention(const void* q, const void* k, const void* v,
                                  float scale, void* out, float* lse,
                                  int32_t* dev_err, cudaStream_t stream);
 
+/*
+ * pkv_stage_from_host - copies a step's inputs from pinned host memory into
+ * device memory with the GPU's own loads. Source: the pages' decode step
+ * copies each step's inputs into the static buffers its captured graph reads,
+ * then replays the graph ("qwen3_flex_inference.py", _decode_step and
+ * capture_decode_cudagraph). On GB300 a copy-engine transfer of such a step's
+ * inputs (under 1 MB) costs ~14 us of mostly fixed latency; read by the SMs
+ * over the coherent host link it takes a few microseconds.
+ *
+ * dst: device (or managed) memory; src: pinned host memory (cudaHostAlloc,
+ * cudaMallocHost or cudaHostRegister; device memory also works); bytes a
+ * multiple of 16, both pointers 16-byte aligned (PKV_ERR_ARG /
+ * PKV_ERR_ALIGN otherwise, nothing launched). Memory the GPU cannot reach
+ * (pageable host memory) is rejected with PKV_ERR_ARG before any launch.
+ * The copy is one kernel on `stream`; a kernel that starts after it on the
+ * stream (a programmatic dependent such as the decode kernels included)
+ * sees the copied bytes. src must not change until the copy has run.
+ */
+pkv_status pkv_stage_from_host(void* dst, const void* src, size_t bytes,
+                               cudaStream_t stream);
+
 /* Static, human-readable name of a status. */
 const char* pkv_status_string(pkv_status status);
 

@@ -9,8 +9,8 @@ Functions keep the names of the C entry points: ``pkv_append``,
 ``pkv_append_rope``, ``pkv_decode_workspace_size``, ``pkv_decode_attention``,
 ``pkv_decode_append_attention``, ``pkv_decode_attention_static_scratch``,
 ``pkv_prefill_attention``, ``pkv_prefill_paged_attention``,
-``pkv_status_string``, ``pkv_status_from_device_error`` and
-``pkv_last_cuda_error_string``.
+``pkv_stage_from_host``, ``pkv_status_string``,
+``pkv_status_from_device_error`` and ``pkv_last_cuda_error_string``.
 """
 
 from __future__ import annotations
@@ -36,7 +36,7 @@ DEV_ERR_TIMEOUT = 0x10
 EXPORTED = ("pkv_append", "pkv_append_rope", "pkv_decode_workspace_size", "pkv_decode_attention",
             "pkv_decode_append_attention", "pkv_decode_attention_static_scratch",
             "pkv_prefill_paged_attention",
-            "pkv_prefill_attention", "pkv_status_string",
+            "pkv_prefill_attention", "pkv_stage_from_host", "pkv_status_string",
             "pkv_status_from_device_error", "pkv_last_cuda_error_string")
 
 
@@ -96,6 +96,8 @@ def load_library() -> ctypes.CDLL:
                                                         i32p, c_int, c_float, vp, f32p, i32p,
                                                         vp]
     lib.pkv_decode_attention_static_scratch.restype = c_int
+    lib.pkv_stage_from_host.argtypes = [vp, vp, c_size, vp]
+    lib.pkv_stage_from_host.restype = c_int
     lib.pkv_status_string.argtypes = [c_int]
     lib.pkv_status_string.restype = ctypes.c_char_p
     lib.pkv_last_cuda_error_string.argtypes = []
@@ -356,3 +358,19 @@ def pkv_prefill_attention(q, k, v, batch_idx, input_pos, scale: float, out=None,
         float(scale), _ptr(out), _ptr(lse), _ptr(dev_err), _stream(stream))
     _check("pkv_prefill_attention", st)
     return out, lse
+
+
+def pkv_stage_from_host(dst: torch.Tensor, src: torch.Tensor, stream=None) -> None:
+    """Copies the bytes of ``src`` (pinned host memory) into ``dst`` (a CUDA
+    tensor of the same byte size) with the GPU's own loads, on the current
+    stream. Both contiguous, 16-byte aligned, size a multiple of 16 bytes."""
+    for name, t in (("dst", dst), ("src", src)):
+        if not isinstance(t, torch.Tensor) or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous tensor")
+    if not dst.is_cuda:
+        raise ValueError("dst must be a CUDA tensor")
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("dst and src must hold the same number of bytes")
+    st = load_library().pkv_stage_from_host(_ptr(dst), _ptr(src), nbytes, _stream(stream))
+    _check("pkv_stage_from_host", st)

@@ -164,3 +164,15 @@ def test_prefill_paged_rejects_bad_arguments(lib):
     assert lib.pkv_prefill_paged_attention(*args(q=264)) == 2
     assert lib.pkv_prefill_paged_attention(*args(n=0)) == 0
     assert lib.pkv_prefill_paged_attention(*args(ps=256, n=0)) == 0
+
+
+def test_stage_from_host_rejects_bad_arguments(lib):
+    """Host checks run before any CUDA call: empty copies succeed, null
+    pointers and sizes off the 16-byte grain are ARG, misaligned pointers
+    ALIGN."""
+    assert lib.pkv_stage_from_host(None, None, 0, None) == 0
+    assert lib.pkv_stage_from_host(None, P(256), 32, None) == 1
+    assert lib.pkv_stage_from_host(P(256), None, 32, None) == 1
+    assert lib.pkv_stage_from_host(P(256), P(512), 24, None) == 1
+    assert lib.pkv_stage_from_host(P(264), P(512), 32, None) == 2
+    assert lib.pkv_stage_from_host(P(256), P(520), 32, None) == 2
