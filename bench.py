@@ -643,6 +643,44 @@ def run_pkv(args):
                 "traffic": (captured_traffic("chunked_prefill_call")
                             if n_decode == 0 and page_size == 128 else None)}
 
+    def timed_mixed_one_call(reps, n_decode=48):
+        """The mixed step (16 chunks of 512 plus `n_decode` decode tokens,
+        shuffled) through pkv_mixed_attention: one call, the decode tokens
+        routed to the split-KV decode kernels; CUDA events over `reps`
+        back-to-back calls (the K/V of the step appended once beforehand)."""
+        c = W.chunked_prefill(0, n_decode=n_decode)
+        q, bi, ip = c.q.to(dev), c.batch_idx.to(dev), c.input_pos.to(dev)
+        kp, vp, pt = c.k_pool.to(dev), c.v_pool.to(dev), c.page_table.to(dev)
+        out = torch.empty_like(q)
+        lse = torch.empty((c.n_tokens, c.num_q_heads), dtype=torch.float32, device=dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        ws = torch.empty(binding.pkv_mixed_workspace_size(kp, pt, c.page_size, c.n_tokens,
+                                                          c.num_q_heads),
+                         dtype=torch.uint8, device=dev)
+        binding.pkv_append(kp, vp, pt, c.k_new.to(dev), c.v_new.to(dev), bi, ip, c.page_size,
+                           dev_err=err)
+
+        def call():
+            binding.pkv_mixed_attention(kp, vp, pt, q, bi, ip, c.page_size, c.scale, out=out,
+                                        lse=lse, workspace=ws, dev_err=err)
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record()
+        for _ in range(reps):
+            call()
+        ev[1].record()
+        torch.cuda.synchronize()
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error bits {int(err.item()):#x} in the one-call mixed step")
+        us = ev[0].elapsed_time(ev[1]) / reps * 1e3
+        flops = 4.0 * c.head_dim * c.num_q_heads * c.info["pairs"]
+        tf = flops / (us * 1e-6) / 1e12
+        return {"call_us": us, "tflops": tf, "frac": tf / bf16_peak,
+                "calls": "pkv_mixed_attention: routing, chunked prefill on the chunks' tokens, "
+                         f"split-KV decode + merge on the {n_decode} decode tokens"}
+
     def timed_mixed_split(reps, n_decode=48):
         """The same mixed step (16 chunks of 512 plus `n_decode` one-token
         decodes, shuffled) served as two calls: the chunks' tokens through the
@@ -741,7 +779,8 @@ def run_pkv(args):
     chunked256 = timed_chunked_prefill(20, page_size=256)
     chunked["mixed_step_with_48_decode_tokens"] = {
         "attention_call_us": mixed["attention_call_us"], "tflops": mixed["tflops"],
-        "frac": mixed["frac"], "split": timed_mixed_split(20)}
+        "frac": mixed["frac"], "split": timed_mixed_split(20),
+        "one_call": timed_mixed_one_call(20)}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -310,6 +310,43 @@ pkv_status pkv_prefill_attention(const void* q, const void* k, const void* v,
                                  int32_t* dev_err, cudaStream_t stream);
 
 /*
+ * pkv_mixed_workspace_size - bytes of device scratch pkv_mixed_attention
+ * needs for n_tokens tokens (0 for invalid arguments).
+ */
+size_t pkv_mixed_workspace_size(const pkv_cache_desc* cache, int n_tokens,
+                                int num_q_heads);
+
+/*
+ * pkv_mixed_attention - one call for a step that interleaves prefill chunks
+ * and decode tokens, each token attending its slot's keys 0..input_pos
+ * through the page table. Source: the step the pages leave on the table,
+ * prefill and decode served in one pass ("flex_vs_vllm.md", "What's left on
+ * the table"); the rule per token is the decode rule
+ * ("qwen3_flex_inference.py", _decode_block_mask, causal_offset).
+ *
+ * Arguments, results and error behaviour are those of
+ * pkv_prefill_paged_attention (the same out and lse, within rounding), plus
+ * a workspace: device scratch of at least pkv_mixed_workspace_size() bytes,
+ * 256-byte aligned, owned by the caller, no initialisation needed; calls
+ * sharing one must be stream-ordered. Inside, tokens that are a run of one
+ * in the packing (a live slot different from both neighbours' slots: decode
+ * tokens) are routed to the split-KV decode kernels, up to 512 of them in
+ * token order; every other token goes through the chunked prefill, where a
+ * lone token would cost a full 128-row product per key tile of its prefix.
+ * Four kernels run on `stream`: the routing, the chunked prefill, the
+ * split-KV decode and its merge. The chunks' and decode tokens' own K/V must
+ * be in the pools already (pkv_append first). page_size must be 16, 32, 64
+ * or a multiple of 128.
+ */
+pkv_status pkv_mixed_attention(const pkv_cache_desc* cache, const void* k_pool,
+                               const void* v_pool, const int32_t* page_table,
+                               const void* q, int num_q_heads,
+                               const int32_t* batch_idx, const int32_t* input_pos,
+                               int n_tokens, float scale, void* out, float* lse,
+                               void* workspace, size_t workspace_bytes,
+                               int32_t* dev_err, cudaStream_t stream);
+
+/*
  * pkv_stage_from_host - copies a step's inputs from pinned host memory into
  * device memory with the GPU's own loads. Source: the pages' decode step
  * copies each step's inputs into the static buffers its captured graph reads,

@@ -9,6 +9,7 @@ Functions keep the names of the C entry points: ``pkv_append``,
 ``pkv_append_rope``, ``pkv_decode_workspace_size``, ``pkv_decode_attention``,
 ``pkv_decode_append_attention``, ``pkv_decode_attention_static_scratch``,
 ``pkv_prefill_attention``, ``pkv_prefill_paged_attention``,
+``pkv_mixed_workspace_size``, ``pkv_mixed_attention``,
 ``pkv_stage_from_host``, ``pkv_status_string``,
 ``pkv_status_from_device_error`` and ``pkv_last_cuda_error_string``.
 """
@@ -36,7 +37,8 @@ DEV_ERR_TIMEOUT = 0x10
 EXPORTED = ("pkv_append", "pkv_append_rope", "pkv_decode_workspace_size", "pkv_decode_attention",
             "pkv_decode_append_attention", "pkv_decode_attention_static_scratch",
             "pkv_prefill_paged_attention",
-            "pkv_prefill_attention", "pkv_stage_from_host", "pkv_status_string",
+            "pkv_prefill_attention", "pkv_mixed_workspace_size", "pkv_mixed_attention",
+            "pkv_stage_from_host", "pkv_status_string",
             "pkv_status_from_device_error", "pkv_last_cuda_error_string")
 
 
@@ -96,6 +98,11 @@ def load_library() -> ctypes.CDLL:
                                                         i32p, c_int, c_float, vp, f32p, i32p,
                                                         vp]
     lib.pkv_decode_attention_static_scratch.restype = c_int
+    lib.pkv_mixed_workspace_size.argtypes = [desc_p, c_int, c_int]
+    lib.pkv_mixed_workspace_size.restype = c_size
+    lib.pkv_mixed_attention.argtypes = [desc_p, vp, vp, i32p, vp, c_int, i32p, i32p, c_int,
+                                        c_float, vp, f32p, vp, c_size, i32p, vp]
+    lib.pkv_mixed_attention.restype = c_int
     lib.pkv_stage_from_host.argtypes = [vp, vp, c_size, vp]
     lib.pkv_stage_from_host.restype = c_int
     lib.pkv_status_string.argtypes = [c_int]
@@ -309,6 +316,47 @@ def pkv_prefill_paged_attention(k_pool, v_pool, page_table, q, batch_idx, input_
         _ptr(batch_idx), _ptr(input_pos), T, float(scale), _ptr(out), _ptr(lse), _ptr(dev_err),
         _stream(stream))
     _check("pkv_prefill_paged_attention", st)
+    return out, lse
+
+
+def pkv_mixed_workspace_size(k_pool, page_table, page_size: int, n_tokens: int,
+                             num_q_heads: int) -> int:
+    desc = cache_desc(k_pool, page_table, page_size)
+    n = load_library().pkv_mixed_workspace_size(ctypes.byref(desc), n_tokens, num_q_heads)
+    if n == 0:
+        raise PkvError("pkv_mixed_workspace_size", 1)
+    return int(n)
+
+
+def pkv_mixed_attention(k_pool, v_pool, page_table, q, batch_idx, input_pos, page_size: int,
+                        scale: float, out=None, lse=None, workspace=None, dev_err=None,
+                        stream=None):
+    """A step of prefill chunks and decode tokens in one call: the results of
+    ``pkv_prefill_paged_attention`` (token i of q [T, Hq, D] attends its
+    slot's keys 0..input_pos[i]), with the decode tokens served by the
+    split-KV decode kernels. Returns (out [T, Hq, D] bf16, lse [T, Hq] fp32)."""
+    _need(q, "q", torch.bfloat16, 3)
+    for name, t, dt, nd in (("k_pool", k_pool, torch.bfloat16, 3),
+                            ("v_pool", v_pool, torch.bfloat16, 3),
+                            ("page_table", page_table, torch.int32, 2),
+                            ("batch_idx", batch_idx, torch.int32, 1),
+                            ("input_pos", input_pos, torch.int32, 1)):
+        _need(t, name, dt, nd)
+    T, hq, d = q.shape
+    if out is None:
+        out = torch.empty((T, hq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, hq), dtype=torch.float32, device=q.device)
+    desc = cache_desc(k_pool, page_table, page_size)
+    lib = load_library()
+    if workspace is None:
+        n = lib.pkv_mixed_workspace_size(ctypes.byref(desc), T, hq)
+        workspace = torch.empty(max(int(n), 256), dtype=torch.uint8, device=q.device)
+    st = lib.pkv_mixed_attention(
+        ctypes.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(q), hq,
+        _ptr(batch_idx), _ptr(input_pos), T, float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_err), _stream(stream))
+    _check("pkv_mixed_attention", st)
     return out, lse
 
 

@@ -171,6 +171,9 @@ pkv_status decode_entry(const pkv_cache_desc* cache, const void* k_pool, const v
   p.v_new = v_new;
   p.k_pool = const_cast<void*>(k_pool);
   p.v_pool = const_cast<void*>(v_pool);
+  p.row_token = nullptr;
+  p.row_count = nullptr;
+  p.input_pos = nullptr;
   p.dev_err = dev_err;
   p.batch = batch;
   p.num_q_heads = num_q_heads;
@@ -183,6 +186,29 @@ pkv_status decode_entry(const pkv_cache_desc* cache, const void* k_pool, const v
   p.qscale = scale * 1.4426950408889634f;
   return cuda_status(pkv::launch_decode(p, kmap, vmap, sms, stream));
 }
+
+// Workspace of pkv_mixed_attention: the routed-token and query-tile counts,
+// the routed tokens (up to `cap`), one skip byte per token, the first token
+// of each prefill query tile, then the decode partials; each part 256-byte
+// aligned.
+struct MixedLayout {
+  int cap;
+  size_t off_list, off_skip, off_seg, off_part, total;
+};
+
+MixedLayout mixed_layout(int n_tokens, int num_kv_heads, int group, int workers) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  MixedLayout m;
+  m.cap = n_tokens < pkv::kDecodeMaxBatch ? n_tokens : pkv::kDecodeMaxBatch;
+  m.off_list = 256;  // [0]: routed count, [1]: query-tile count
+  m.off_skip = m.off_list + up(static_cast<size_t>(m.cap) * 4);
+  m.off_seg = m.off_skip + up(static_cast<size_t>(n_tokens));
+  m.off_part = m.off_seg + up(static_cast<size_t>(n_tokens) * 4);
+  m.total = m.off_part + pkv::decode_workspace_bytes(m.cap, num_kv_heads, group, workers);
+  return m;
+}
+
+bool paged_page_size_ok(int ps) { return ps == 16 || ps == 32 || ps == 64 || ps % 128 == 0; }
 
 }  // namespace
 
@@ -342,6 +368,96 @@ pkv_status pkv_prefill_paged_attention(const pkv_cache_desc* cache, const void* 
   if (st != PKV_OK) return st;
   return pkv::prefill_paged_entry(cache, k_pool, v_pool, page_table, q, num_q_heads, batch_idx,
                                   input_pos, n_tokens, scale, out, lse, dev_err, stream);
+}
+
+size_t pkv_mixed_workspace_size(const pkv_cache_desc* cache, int n_tokens, int num_q_heads) {
+  if (check_cache(cache) != PKV_OK || n_tokens < 0) return 0;
+  if (!group_ok(num_q_heads, cache->num_kv_heads)) return 0;
+  int sms = 0;
+  if (device_info(&sms) != PKV_OK) return 0;
+  return mixed_layout(n_tokens, cache->num_kv_heads, num_q_heads / cache->num_kv_heads,
+                      pkv::decode_workers_for_device(sms))
+      .total;
+}
+
+pkv_status pkv_mixed_attention(const pkv_cache_desc* cache, const void* k_pool,
+                               const void* v_pool, const int32_t* page_table, const void* q,
+                               int num_q_heads, const int32_t* batch_idx,
+                               const int32_t* input_pos, int n_tokens, float scale, void* out,
+                               float* lse, void* workspace, size_t workspace_bytes,
+                               int32_t* dev_err, cudaStream_t stream) {
+  // every check of both kernels runs here, before anything is launched
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (!paged_page_size_ok(cache->page_size)) return PKV_ERR_ARG;
+  if (!group_ok(num_q_heads, cache->num_kv_heads)) return PKV_ERR_ARG;
+  if (n_tokens < 0 || !std::isfinite(scale) || !(scale > 0.f)) return PKV_ERR_ARG;
+  if (n_tokens == 0) return PKV_OK;
+  if (!k_pool || !v_pool || !page_table || !q || !batch_idx || !input_pos || !out || !lse)
+    return PKV_ERR_ARG;
+  if (!aligned(k_pool, 16) || !aligned(v_pool, 16) || !aligned(q, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4) || !aligned(page_table, 4) || !aligned(batch_idx, 4) ||
+      !aligned(input_pos, 4) || !aligned(dev_err, 4))
+    return PKV_ERR_ALIGN;
+  if (static_cast<long long>(((n_tokens + 127) / 128)) * num_q_heads > INT_MAX)
+    return PKV_ERR_ARG;
+  int sms = 0;
+  st = device_info(&sms);
+  if (st != PKV_OK) return st;
+  const int group = num_q_heads / cache->num_kv_heads;
+  const int workers = pkv::decode_workers_for_device(sms);
+  const MixedLayout lay = mixed_layout(n_tokens, cache->num_kv_heads, group, workers);
+  if (workspace == nullptr || workspace_bytes < lay.total) return PKV_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return PKV_ERR_ALIGN;
+  CUtensorMap kmap, vmap;
+  st = encode_pool_map(&kmap, k_pool, cache);
+  if (st != PKV_OK) return st;
+  st = encode_pool_map(&vmap, v_pool, cache);
+  if (st != PKV_OK) return st;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* count = reinterpret_cast<int32_t*>(ws);
+  int32_t* seg_count = count + 1;
+  int32_t* list = reinterpret_cast<int32_t*>(ws + lay.off_list);
+  uint8_t* skip = ws + lay.off_skip;
+  int32_t* seg_start = reinterpret_cast<int32_t*>(ws + lay.off_seg);
+  // 1. the tokens that are a run of one, listed and flagged, and the query
+  //    tiles of the others
+  cudaError_t e = pkv::launch_route_lone(batch_idx, n_tokens, lay.cap, list, count, skip,
+                                         seg_start, seg_count, stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  // 2. every other token through the chunked prefill, tiled by run pieces
+  st = pkv::prefill_paged_entry(cache, k_pool, v_pool, page_table, q, num_q_heads, batch_idx,
+                                input_pos, n_tokens, scale, out, lse, dev_err, stream, skip,
+                                seg_start, seg_count);
+  if (st != PKV_OK) return st;
+  // 3. the listed tokens through the split-KV decode and its merge
+  pkv::DecodeParams p;
+  p.q = q;
+  p.page_table = page_table;
+  p.batch_idx = batch_idx;
+  p.seq_lens = nullptr;
+  p.out = out;
+  p.lse = lse;
+  p.partials = reinterpret_cast<float*>(ws + lay.off_part);
+  p.k_new = nullptr;
+  p.v_new = nullptr;
+  p.k_pool = const_cast<void*>(k_pool);
+  p.v_pool = const_cast<void*>(v_pool);
+  p.row_token = list;
+  p.row_count = count;
+  p.input_pos = input_pos;
+  p.dev_err = dev_err;
+  p.batch = lay.cap;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = cache->num_kv_heads;
+  p.page_size = cache->page_size;
+  p.num_pages = cache->num_pages;
+  p.max_batch = cache->max_batch;
+  p.max_blocks = cache->max_blocks;
+  p.num_workers = workers;
+  p.qscale = scale * 1.4426950408889634f;
+  return cuda_status(pkv::launch_decode(p, kmap, vmap, sms, stream));
 }
 
 pkv_status pkv_prefill_attention(const void* q, const void* k, const void* v, int num_q_heads,

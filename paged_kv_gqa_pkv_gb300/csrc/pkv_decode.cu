@@ -64,10 +64,11 @@ struct DecodeCfg {
   static constexpr int kBarOffset = kDecodeWarps * kStages * kStageStride;
   static constexpr int kWarpSumOffset = kBarOffset + kDecodeWarps * kStages * 8;
   static constexpr int kRowsOffset = kWarpSumOffset + kDecodeWarps * 4;
-  static constexpr size_t smem_bytes(int batch) {
-    // seq_len and slot per row, the tile prefix over rows ([batch + 1]), and
-    // 1 KB to round the dynamic base up to the swizzle-atom alignment
-    return 1024 + kRowsOffset + static_cast<size_t>(batch) * 8 +
+  static constexpr size_t smem_bytes(int batch, bool list = false) {
+    // seq_len and slot per row, the tile prefix over rows ([batch + 1]), the
+    // row's token in list mode, and 1 KB to round the dynamic base up to the
+    // swizzle-atom alignment
+    return 1024 + kRowsOffset + static_cast<size_t>(batch) * (list ? 12 : 8) +
            static_cast<size_t>(batch + 1) * 4;
   }
 };
@@ -81,12 +82,37 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
                                (((chunk & 7) ^ (row & 7)) << 4));
 }
 
+// Slot c, keys attended n and token t of row r: the call's row r, or in
+// list mode (kList) the packed token t = row_token[r], which attends
+// input_pos[t] + 1 keys (a negative position counts as out of range).
+template <bool kList>
+__device__ __forceinline__ void row_input(const DecodeParams& p, int r, int& c, int& n, int& t) {
+  if constexpr (kList) {
+    t = p.row_token[r];
+    c = p.batch_idx[t];
+    const int pos = p.input_pos[t];
+    n = pos < 0 ? -1 : pos + 1;
+  } else {
+    t = r;
+    c = p.batch_idx[r];
+    n = p.seq_lens[r];
+  }
+}
+
+// Rows of the call: the batch, or in list mode the device-side count.
+template <bool kList>
+__device__ __forceinline__ int call_rows(const DecodeParams& p) {
+  if constexpr (kList) return min(max(*p.row_count, 0), p.batch);
+  return p.batch;
+}
+
 // Tiles of row r and the device error its entries raise (0 if none). Both
 // kernels apply this one rule, so the merge can rebuild the split-KV pass's
 // schedule from the call's inputs alone.
+template <bool kList>
 __device__ __forceinline__ int row_tiles(const DecodeParams& p, int r, int* err) {
-  const int c = p.batch_idx[r];
-  const int n = p.seq_lens[r];
+  int c, n, t;
+  row_input<kList>(p, r, c, n, t);
   *err = 0;
   if (c < 0 || c >= p.max_batch) *err = PKV_DEV_ERR_BAD_SLOT;
   else if (n < 0 || n > p.max_blocks * p.page_size) *err = PKV_DEV_ERR_BAD_POS;
@@ -263,7 +289,7 @@ __device__ __forceinline__ void combine_segments(const DecodeParams& p, int b, i
 // kCombine: the launch expects long items (few rows for the machine) and the
 // CTAs combine their partials of those; without it the code below it is
 // compiled out and every item goes to the merge kernel one segment per warp.
-template <int G, bool kCombine>
+template <int G, bool kCombine, bool kList>
 __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const DecodeParams p) {
@@ -277,7 +303,7 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-  const int B = p.batch;
+  const int B = call_rows<kList>(p);
   const int hkv = p.num_kv_heads;
 
   uint8_t* stages = smem + warp * S * C::kStageStride;
@@ -286,6 +312,7 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
   int32_t* s_len = reinterpret_cast<int32_t*>(smem + C::kRowsOffset);
   int32_t* s_slot = s_len + B;
   int32_t* s_prefix = s_slot + B;
+  int32_t* s_tok = s_prefix + B + 1;  // list mode: token of each row
 
   if (lane == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
@@ -307,11 +334,13 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
   const int r1 = min(r0 + per_thread, B);
   int local = 0;
   for (int r = r0; r < r1; ++r) {
-    int err;
-    const int tiles = row_tiles(p, r, &err);
+    int err, c, n, t;
+    const int tiles = row_tiles<kList>(p, r, &err);
     if (err && blockIdx.x == 0) set_dev_err(p.dev_err, err);
-    s_len[r] = p.seq_lens[r];
-    s_slot[r] = p.batch_idx[r];
+    row_input<kList>(p, r, c, n, t);
+    s_len[r] = n;
+    s_slot[r] = c;
+    if constexpr (kList) s_tok[r] = t;
     s_prefix[r] = tiles;
     local += tiles;
   }
@@ -376,8 +405,9 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
       tma_load_4d(st, &kmap, &bars[s], 0, row, 0, c.kvh);
       tma_load_4d(st + C::kOffV, &vmap, &bars[s], 0, row, 0, c.kvh);
       if (seg_start) {
+        const int qrow = kList ? s_tok[c.b] : c.b;
         const size_t qoff =
-            (static_cast<size_t>(c.b) * p.num_q_heads + static_cast<size_t>(c.kvh) * G) *
+            (static_cast<size_t>(qrow) * p.num_q_heads + static_cast<size_t>(c.kvh) * G) *
             kHeadDim * 2;
         bulk_load(st + C::kOffQ, qbase + qoff, C::kQBytes, &bars[s]);
       }
@@ -549,7 +579,8 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
         // the item lies in this segment alone: normalise and write it out
         // here (the merge skips items of one segment)
         const float inv0 = 1.f / lt0, inv1 = 1.f / lt1;
-        const int64_t head0 = static_cast<int64_t>(cc.b) * p.num_q_heads + cc.kvh * G + 2 * t;
+        const int orow = kList ? s_tok[cc.b] : cc.b;
+        const int64_t head0 = static_cast<int64_t>(orow) * p.num_q_heads + cc.kvh * G + 2 * t;
         __nv_bfloat16* o0 = static_cast<__nv_bfloat16*>(p.out) + head0 * kHeadDim + g;
         __nv_bfloat16* o1 = o0 + kHeadDim;
 #pragma unroll
@@ -672,7 +703,7 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
 // split-KV grid, so after the wait only the partials are read: for items of
 // up to kFast segments (16 with kByCta, else 8), (m, l) and all o rows go out
 // in one round of loads.
-template <int G, bool kByCta>
+template <int G, bool kByCta, bool kList>
 __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p) {
   constexpr int kFast = kByCta ? 16 : 8;
   // The next launch may start its prologue now; it touches the workspace
@@ -680,7 +711,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int wid = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int B = p.batch;
+  const int B = call_rows<kList>(p);
   const bool active = wid < B * p.num_q_heads;
   const int b = active ? wid / p.num_q_heads : 0;
   const int h = wid % p.num_q_heads;
@@ -690,7 +721,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
   int before = 0, total = 0, tiles = 0;
   for (int r = lane; r < B; r += 32) {
     int err;
-    const int t = row_tiles(p, r, &err);
+    const int t = row_tiles<kList>(p, r, &err);
     total += t;
     if (r < b) before += t;
     if (r == b) tiles = t;
@@ -703,11 +734,13 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
   }
   pdl_wait_primary();
   if (!active) return;
-  __nv_bfloat16* out =
-      static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(wid) * kHeadDim + lane * 4;
+  // output row of (b, h): wid itself, or in list mode that of b's token
+  const int64_t oid =
+      kList ? static_cast<int64_t>(p.row_token[b]) * p.num_q_heads + h : static_cast<int64_t>(wid);
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + oid * kHeadDim + lane * 4;
   if (tiles == 0) {
     *reinterpret_cast<uint2*>(out) = make_uint2(0u, 0u);
-    if (lane == 0) p.lse[wid] = -INFINITY;
+    if (lane == 0) p.lse[oid] = -INFINITY;
     return;
   }
   const int64_t per = (static_cast<int64_t>(total) * hkv + p.num_workers - 1) / p.num_workers;
@@ -795,7 +828,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p)
   packed.x = *reinterpret_cast<const uint32_t*>(&lo);
   packed.y = *reinterpret_cast<const uint32_t*>(&hi);
   *reinterpret_cast<uint2*>(out) = packed;
-  if (lane == 0) p.lse[wid] = (M + log2f(L)) * 0.69314718055994531f;
+  if (lane == 0) p.lse[oid] = (M + log2f(L)) * 0.69314718055994531f;
 }
 
 size_t decode_workspace_bytes(int batch, int num_kv_heads, int group, int num_workers) {
@@ -806,12 +839,12 @@ size_t decode_workspace_bytes(int batch, int num_kv_heads, int group, int num_wo
 
 int decode_workers_for_device(int sm_count) { return sm_count * kDecodeWarps; }
 
-template <int G, bool kCombine>
+template <int G, bool kCombine, bool kList>
 static cudaError_t launch_decode_gc(const DecodeParams& p, const CUtensorMap& kmap,
                                     const CUtensorMap& vmap, int sm_count, cudaStream_t stream) {
   using C = DecodeCfg<G>;
-  const size_t smem = C::smem_bytes(p.batch);
-  static_assert(C::smem_bytes(kDecodeMaxBatch) <= 232448, "decode shared memory over budget");
+  const size_t smem = C::smem_bytes(p.batch, kList);
+  static_assert(C::smem_bytes(kDecodeMaxBatch, true) <= 232448, "decode shared memory over budget");
   // The shared-memory opt-in is set once per device, so steady-state calls
   // (and calls under stream capture) only enqueue kernels.
   static std::atomic<bool> attr_set[64] = {};  // per device; host threads may race to set it
@@ -820,18 +853,18 @@ static cudaError_t launch_decode_gc(const DecodeParams& p, const CUtensorMap& km
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(decode_splitkv_kernel<G, kCombine>,
+    e = cudaFuncSetAttribute(decode_splitkv_kernel<G, kCombine, kList>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(C::smem_bytes(kDecodeMaxBatch)));
+                             static_cast<int>(C::smem_bytes(kDecodeMaxBatch, kList)));
     if (e != cudaSuccess) return e;
     attr_set[dev].store(true, std::memory_order_release);
   }
-  e = launch_kernel(decode_splitkv_kernel<G, kCombine>, dim3(sm_count), dim3(kDecodeWarps * 32),
-                    smem, stream, /*programmatic=*/true, kmap, vmap, p);
+  e = launch_kernel(decode_splitkv_kernel<G, kCombine, kList>, dim3(sm_count),
+                    dim3(kDecodeWarps * 32), smem, stream, /*programmatic=*/true, kmap, vmap, p);
   if (e != cudaSuccess) return e;
   const int rows = p.batch * p.num_q_heads;
-  return launch_kernel(decode_merge_kernel<G, kCombine>, dim3((rows + 7) / 8), dim3(256), 0,
-                       stream, /*programmatic=*/true, p);
+  return launch_kernel(decode_merge_kernel<G, kCombine, kList>, dim3((rows + 7) / 8), dim3(256),
+                       0, stream, /*programmatic=*/true, p);
 }
 
 // Few (row, kv head) items for the machine's workers means long items: then
@@ -841,8 +874,11 @@ static cudaError_t launch_decode_g(const DecodeParams& p, const CUtensorMap& kma
                                    const CUtensorMap& vmap, int sm_count, cudaStream_t stream) {
   const bool combine =
       static_cast<int64_t>(p.batch) * p.num_kv_heads * kLongItemSegs < p.num_workers;
-  return combine ? launch_decode_gc<G, true>(p, kmap, vmap, sm_count, stream)
-                 : launch_decode_gc<G, false>(p, kmap, vmap, sm_count, stream);
+  if (p.row_token != nullptr)
+    return combine ? launch_decode_gc<G, true, true>(p, kmap, vmap, sm_count, stream)
+                   : launch_decode_gc<G, false, true>(p, kmap, vmap, sm_count, stream);
+  return combine ? launch_decode_gc<G, true, false>(p, kmap, vmap, sm_count, stream)
+                 : launch_decode_gc<G, false, false>(p, kmap, vmap, sm_count, stream);
 }
 
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,

@@ -60,6 +60,13 @@ struct DecodeParams {
   const void* v_new;
   void* k_pool;               // the pools as written (the tensor maps read them)
   void* v_pool;
+  // Token list (all null for the usual rows): row r serves packed token
+  // t = row_token[r] of a prefill-style call. Its slot is batch_idx[t], it
+  // attends input_pos[t] + 1 keys, and q, out and lse are indexed by t. The
+  // number of rows is min(*row_count, batch), read on the device.
+  const int32_t* row_token;
+  const int32_t* row_count;
+  const int32_t* input_pos;
   int32_t* dev_err;
   int batch;
   int num_q_heads;
@@ -102,13 +109,30 @@ pkv_status prefill_entry(const void* q, const void* k, const void* v, int num_q_
                          const int32_t* input_pos, int n_tokens, float scale, void* out,
                          float* lse, int32_t* dev_err, cudaStream_t stream);
 
+// Validation and launch of pkv_prefill_paged_attention (pkv_prefill_paged.cu).
+// skip (nullable, one byte per token): tokens with a nonzero byte are left
+// out entirely (no keys, nothing written); another kernel serves them.
+// seg_start/seg_count (nullable, device): query tiles start at these tokens
+// and cover the run of equal slots from there (at most 128 tokens) instead of
+// fixed 128-token windows of the packing.
 pkv_status prefill_paged_entry(const pkv_cache_desc* cache, const void* k_pool,
                                const void* v_pool, const int32_t* page_table, const void* q,
                                int num_q_heads, const int32_t* batch_idx,
                                const int32_t* input_pos, int n_tokens, float scale, void* out,
-                               float* lse, int32_t* dev_err, cudaStream_t stream);
+                               float* lse, int32_t* dev_err, cudaStream_t stream,
+                               const uint8_t* skip = nullptr, const int32_t* seg_start = nullptr,
+                               const int32_t* seg_count = nullptr);
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           int sm_count, cudaStream_t stream);
+
+// pkv_mixed.cu: lists the first `cap` tokens that are a run of one in the
+// packing (ascending) in list[0, *count) and sets skip[i] = 1 for each of them
+// (0 for every other token); lists the first tokens of the prefill kernel's
+// query tiles (pieces of at most 128 tokens of each run of equal slots, the
+// listed tokens left out) in seg_start[0, *seg_count).
+cudaError_t launch_route_lone(const int32_t* batch_idx, int n_tokens, int cap, int32_t* list,
+                              int32_t* count, uint8_t* skip, int32_t* seg_start,
+                              int32_t* seg_count, cudaStream_t stream);
 
 // cudaLaunchKernelEx with an optional programmatic-stream-serialisation
 // attribute (programmatic dependent launch).

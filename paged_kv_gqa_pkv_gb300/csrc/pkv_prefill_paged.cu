@@ -70,6 +70,11 @@ struct PagedPrefillParams {
   const int32_t* page_table;
   const int32_t* batch_idx;
   const int32_t* input_pos;
+  const uint8_t* skip;  // nullable: tokens served elsewhere (nothing written here)
+  // nullable: query tiles start at seg_start[0, *seg_count) and cover the run
+  // of equal slots from there (at most 128 rows), instead of 128-row windows
+  const int32_t* seg_start;
+  const int32_t* seg_count;
   void* out;
   float* lse;
   int32_t* dev_err;
@@ -87,14 +92,16 @@ struct PagedPrefillParams {
   float qscale;         // scale * log2(e)
 };
 
-// Slot and position of a row, or slot 0 for padding and for a rejected row
-// (slot outside the table, position outside [0, max_blocks * page_size)).
+// Slot and position of a row, or slot 0 for padding, for a rejected row
+// (slot outside the table, position outside [0, max_blocks * page_size)) and
+// for a token another kernel serves (skip).
 __device__ __forceinline__ void row_meta(const PagedPrefillParams& p, int i, int& b, int& pos,
                                          int& err) {
   b = 0;
   pos = 0;
   err = 0;
   if (i < 0 || i >= p.n_tokens) return;
+  if (p.skip != nullptr && __ldg(p.skip + i) != 0) return;
   const int bb = __ldg(p.batch_idx + i);
   const int pp = __ldg(p.input_pos + i);
   if (bb == 0) return;
@@ -106,17 +113,35 @@ __device__ __forceinline__ void row_meta(const PagedPrefillParams& p, int i, int
 }
 
 // One warp's view of a query tile's 128 rows: lane l holds rows l + 32 m.
+// The tile starts at token r0; its first `len` rows are its own (all 128 for
+// the usual tiles; with listed tile starts, the leading rows whose slot, as
+// given, equals the first row's). Rows past len are no part of the tile.
 struct TileRows {
   int b[4];
   int pos[4];
+  int r0;
+  int len;
 };
 
 __device__ __forceinline__ TileRows tile_rows_load(const PagedPrefillParams& p, int r0, int lane) {
   TileRows t;
+  t.r0 = r0;
+  t.len = kBM;
+  if (p.seg_start != nullptr && r0 >= 0) {
+    const int b0 = __ldg(p.batch_idx + r0);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int i = r0 + lane + 32 * m;
+      const uint32_t brk =
+          __ballot_sync(0xffffffffu, i >= p.n_tokens || __ldg(p.batch_idx + i) != b0);
+      if (brk != 0u) t.len = min(t.len, 32 * m + __ffs(brk) - 1);
+    }
+  }
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
     int err;
-    row_meta(p, r0 >= 0 ? r0 + lane + 32 * m : -1, t.b[m], t.pos[m], err);
+    const int row = lane + 32 * m;
+    row_meta(p, r0 >= 0 && row < t.len ? r0 + row : -1, t.b[m], t.pos[m], err);
   }
   return t;
 }
@@ -212,8 +237,18 @@ __device__ __forceinline__ int count_tiles(const TileRows& t, const RunMasks& rm
   return n;
 }
 
-__device__ __forceinline__ int item_r0(const PagedPrefillParams& p, int item, int items_per_tile) {
-  return item < p.n_items ? (item / items_per_tile) * kBM : -1;
+// Items of the call: tiles x head groups; with listed tile starts the tile
+// count is read on the device.
+__device__ __forceinline__ int call_items(const PagedPrefillParams& p, int items_per_tile) {
+  return p.seg_start != nullptr ? *p.seg_count * items_per_tile : p.n_items;
+}
+
+// First token of an item's query tile (-1 past the last item).
+__device__ __forceinline__ int item_r0(const PagedPrefillParams& p, int item, int items_per_tile,
+                                       int n_items) {
+  if (item >= n_items) return -1;
+  const int tile = item / items_per_tile;
+  return p.seg_start != nullptr ? __ldg(p.seg_start + tile) : tile * kBM;
 }
 
 }  // namespace
@@ -244,6 +279,7 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
   const int lane = threadIdx.x & 31;
   const int hpi = p.heads_per_item;
   const int items_per_tile = p.num_q_heads / hpi;
+  const int n_items = call_items(p, items_per_tile);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -278,14 +314,13 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
     uint32_t qi = 0;  // non-empty items
     const int R = p.box_rows;
     const int nsub = kBN / R;  // boxes per head-dim half of a key tile (1..8)
-    TileRows nxt = tile_rows_load(p, item_r0(p, blockIdx.x, items_per_tile), lane);
-    for (int item = blockIdx.x; item < p.n_items && !*s_abort; item += gridDim.x) {
-      const int tile = item / items_per_tile;
+    TileRows nxt = tile_rows_load(p, item_r0(p, blockIdx.x, items_per_tile, n_items), lane);
+    for (int item = blockIdx.x; item < n_items && !*s_abort; item += gridDim.x) {
       const int h0 = (item % items_per_tile) * hpi;
       const int kvh = h0 / p.group;
-      const int r0 = tile * kBM;
       const TileRows cur = nxt;
-      nxt = tile_rows_load(p, item_r0(p, item + gridDim.x, items_per_tile), lane);
+      const int r0 = cur.r0;
+      nxt = tile_rows_load(p, item_r0(p, item + gridDim.x, items_per_tile, n_items), lane);
       const RunMasks rm = run_masks(cur, lane);
       const int n_kv = count_tiles(cur, rm, lane);
       if (n_kv == 0) continue;
@@ -399,10 +434,10 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
       if (elect_one()) umma_commit(bar);
       __syncwarp();
     };
-    TileRows nxt = tile_rows_load(p, item_r0(p, blockIdx.x, items_per_tile), lane);
-    for (int item = blockIdx.x; item < p.n_items && !*s_abort; item += gridDim.x) {
+    TileRows nxt = tile_rows_load(p, item_r0(p, blockIdx.x, items_per_tile, n_items), lane);
+    for (int item = blockIdx.x; item < n_items && !*s_abort; item += gridDim.x) {
       const TileRows cur = nxt;
-      nxt = tile_rows_load(p, item_r0(p, item + gridDim.x, items_per_tile), lane);
+      nxt = tile_rows_load(p, item_r0(p, item + gridDim.x, items_per_tile, n_items), lane);
       const RunMasks rm = run_masks(cur, lane);
       const int n_kv = count_tiles(cur, rm, lane);
       if (n_kv == 0) continue;
@@ -492,19 +527,19 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
     const uint32_t t_o = tmem + (static_cast<uint32_t>(lane_base) << 16) + 256 + grp * kHeadDim;
     uint32_t tc = 0, qi = 0;
     const bool active = grp < hpi;
-    TileRows nxt = tile_rows_load(p, item_r0(p, blockIdx.x, items_per_tile), lane);
-    for (int item = blockIdx.x; active && item < p.n_items; item += gridDim.x) {
+    TileRows nxt = tile_rows_load(p, item_r0(p, blockIdx.x, items_per_tile, n_items), lane);
+    for (int item = blockIdx.x; active && item < n_items; item += gridDim.x) {
       if (__any_sync(0xffffffffu, *s_abort != 0)) break;  // warp-uniform exit
-      const int tile = item / items_per_tile;
       const int head = (item % items_per_tile) * hpi + grp;
-      const int r0 = tile * kBM;
       const TileRows cur = nxt;
-      nxt = tile_rows_load(p, item_r0(p, item + gridDim.x, items_per_tile), lane);
+      const int r0 = cur.r0;
+      nxt = tile_rows_load(p, item_r0(p, item + gridDim.x, items_per_tile, n_items), lane);
       const RunMasks rm = run_masks(cur, lane);
       const int n_kv = count_tiles(cur, rm, lane);
       const int i = r0 + row;
+      const bool mine = row < cur.len;  // the row belongs to this tile
       int my_b, my_pos, my_err;
-      row_meta(p, i, my_b, my_pos, my_err);
+      row_meta(p, mine ? i : -1, my_b, my_pos, my_err);
       if (my_err && grp == 0) set_dev_err(p.dev_err, my_err);
       float m_run = -INFINITY;  // running max, raw score units
       float l_run = 0.f;
@@ -589,7 +624,9 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
         if (!__all_sync(0xffffffffu, got)) ok = false;
       }
       tc_fence_after();
-      const bool in_range = i < p.n_tokens;
+      // tokens served by another kernel are not written here
+      const bool in_range =
+          mine && i < p.n_tokens && !(p.skip != nullptr && __ldg(p.skip + i) != 0);
       const bool has = in_range && my_b != 0 && ok && l_run > 0.f;
       const float inv = has ? 1.f / l_run : 0.f;
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
@@ -654,7 +691,9 @@ pkv_status prefill_paged_entry(const pkv_cache_desc* cache, const void* k_pool,
                                const void* v_pool, const int32_t* page_table, const void* q,
                                int num_q_heads, const int32_t* batch_idx,
                                const int32_t* input_pos, int n_tokens, float scale, void* out,
-                               float* lse, int32_t* dev_err, cudaStream_t stream) {
+                               float* lse, int32_t* dev_err, cudaStream_t stream,
+                               const uint8_t* skip, const int32_t* seg_start,
+                               const int32_t* seg_count) {
   if (cache == nullptr || cache->head_dim != kHeadDim || cache->num_pages <= 0 ||
       cache->num_kv_heads <= 0 || cache->max_batch <= 0 || cache->max_blocks <= 0)
     return PKV_ERR_ARG;
@@ -706,6 +745,9 @@ pkv_status prefill_paged_entry(const pkv_cache_desc* cache, const void* k_pool,
   prm.page_table = page_table;
   prm.batch_idx = batch_idx;
   prm.input_pos = input_pos;
+  prm.skip = skip;
+  prm.seg_start = seg_count != nullptr ? seg_start : nullptr;
+  prm.seg_count = seg_count;
   prm.out = out;
   prm.lse = lse;
   prm.dev_err = dev_err;
@@ -721,7 +763,11 @@ pkv_status prefill_paged_entry(const pkv_cache_desc* cache, const void* k_pool,
   prm.max_blocks = cache->max_blocks;
   prm.box_rows = box_rows;
   prm.qscale = scale * 1.4426950408889634f;
-  const int grid = prm.n_items < sms ? prm.n_items : sms;
+  // with listed tile starts there are at most n_tokens tiles
+  const long long items_max =
+      prm.seg_start != nullptr ? static_cast<long long>(n_tokens) * (num_q_heads / prm.heads_per_item)
+                               : prm.n_items;
+  const int grid = items_max < sms ? static_cast<int>(items_max) : sms;
   const cudaError_t e = launch_kernel(prefill_paged_tcgen05_kernel, dim3(grid), dim3(kThreads),
                                       kSmemBytes, stream, false, qmap, kmap, vmap, prm);
   return record_cuda_status(e);

@@ -176,3 +176,16 @@ def test_stage_from_host_rejects_bad_arguments(lib):
     assert lib.pkv_stage_from_host(P(256), P(512), 24, None) == 1
     assert lib.pkv_stage_from_host(P(264), P(512), 32, None) == 2
     assert lib.pkv_stage_from_host(P(256), P(520), 32, None) == 2
+
+
+def test_mixed_rejects_bad_arguments(lib):
+    d = _desc()
+    args = lambda ps=16, hq=8, n=4, q=256, ws=256: (  # noqa: E731
+        ctypes.byref(_desc(page_size=ps)), P(256), P(256), P(256), P(q), hq, P(256), P(256), n,
+        ctypes.c_float(0.088), P(256), P(256), P(ws), 1 << 20, None, None)
+    assert lib.pkv_mixed_attention(*args(ps=48)) == 1      # page size the prefill side refuses
+    assert lib.pkv_mixed_attention(*args(hq=12)) == 1      # GQA group of 6
+    assert lib.pkv_mixed_attention(*args(n=-1)) == 1
+    assert lib.pkv_mixed_attention(*args(n=0)) == 0
+    assert lib.pkv_mixed_attention(*args(q=264)) == 2
+    assert lib.pkv_mixed_workspace_size(ctypes.byref(d), -1, 8) == 0
