@@ -123,11 +123,12 @@ struct TileRows {
   int len;
 };
 
+template <bool kSeg>
 __device__ __forceinline__ TileRows tile_rows_load(const PagedPrefillParams& p, int r0, int lane) {
   TileRows t;
   t.r0 = r0;
   t.len = kBM;
-  if (p.seg_start != nullptr && r0 >= 0) {
+  if (kSeg && r0 >= 0) {
     const int b0 = __ldg(p.batch_idx + r0);
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
@@ -239,22 +240,27 @@ __device__ __forceinline__ int count_tiles(const TileRows& t, const RunMasks& rm
 
 // Items of the call: tiles x head groups; with listed tile starts the tile
 // count is read on the device.
+template <bool kSeg>
 __device__ __forceinline__ int call_items(const PagedPrefillParams& p, int items_per_tile) {
-  return p.seg_start != nullptr ? *p.seg_count * items_per_tile : p.n_items;
+  return kSeg ? *p.seg_count * items_per_tile : p.n_items;
 }
 
 // First token of an item's query tile (-1 past the last item).
+template <bool kSeg>
 __device__ __forceinline__ int item_r0(const PagedPrefillParams& p, int item, int items_per_tile,
                                        int n_items) {
   if (item >= n_items) return -1;
   const int tile = item / items_per_tile;
-  return p.seg_start != nullptr ? __ldg(p.seg_start + tile) : tile * kBM;
+  return kSeg ? __ldg(p.seg_start + tile) : tile * kBM;
 }
 
 }  // namespace
 
 // 10 warps: two of the four SM sub-partitions hold three warps, so at most
 // 16384 / 96 = 170 registers per thread
+// kSeg: query tiles start at the listed tokens (p.seg_start) and cover one
+// run piece each; else they are fixed 128-row windows of the packing.
+template <bool kSeg>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
                              const __grid_constant__ CUtensorMap kmap,
@@ -279,7 +285,7 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
   const int lane = threadIdx.x & 31;
   const int hpi = p.heads_per_item;
   const int items_per_tile = p.num_q_heads / hpi;
-  const int n_items = call_items(p, items_per_tile);
+  const int n_items = call_items<kSeg>(p, items_per_tile);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -314,13 +320,13 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
     uint32_t qi = 0;  // non-empty items
     const int R = p.box_rows;
     const int nsub = kBN / R;  // boxes per head-dim half of a key tile (1..8)
-    TileRows nxt = tile_rows_load(p, item_r0(p, blockIdx.x, items_per_tile, n_items), lane);
+    TileRows nxt = tile_rows_load<kSeg>(p, item_r0<kSeg>(p, blockIdx.x, items_per_tile, n_items), lane);
     for (int item = blockIdx.x; item < n_items && !*s_abort; item += gridDim.x) {
       const int h0 = (item % items_per_tile) * hpi;
       const int kvh = h0 / p.group;
       const TileRows cur = nxt;
       const int r0 = cur.r0;
-      nxt = tile_rows_load(p, item_r0(p, item + gridDim.x, items_per_tile, n_items), lane);
+      nxt = tile_rows_load<kSeg>(p, item_r0<kSeg>(p, item + gridDim.x, items_per_tile, n_items), lane);
       const RunMasks rm = run_masks(cur, lane);
       const int n_kv = count_tiles(cur, rm, lane);
       if (n_kv == 0) continue;
@@ -434,10 +440,10 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
       if (elect_one()) umma_commit(bar);
       __syncwarp();
     };
-    TileRows nxt = tile_rows_load(p, item_r0(p, blockIdx.x, items_per_tile, n_items), lane);
+    TileRows nxt = tile_rows_load<kSeg>(p, item_r0<kSeg>(p, blockIdx.x, items_per_tile, n_items), lane);
     for (int item = blockIdx.x; item < n_items && !*s_abort; item += gridDim.x) {
       const TileRows cur = nxt;
-      nxt = tile_rows_load(p, item_r0(p, item + gridDim.x, items_per_tile, n_items), lane);
+      nxt = tile_rows_load<kSeg>(p, item_r0<kSeg>(p, item + gridDim.x, items_per_tile, n_items), lane);
       const RunMasks rm = run_masks(cur, lane);
       const int n_kv = count_tiles(cur, rm, lane);
       if (n_kv == 0) continue;
@@ -527,13 +533,13 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
     const uint32_t t_o = tmem + (static_cast<uint32_t>(lane_base) << 16) + 256 + grp * kHeadDim;
     uint32_t tc = 0, qi = 0;
     const bool active = grp < hpi;
-    TileRows nxt = tile_rows_load(p, item_r0(p, blockIdx.x, items_per_tile, n_items), lane);
+    TileRows nxt = tile_rows_load<kSeg>(p, item_r0<kSeg>(p, blockIdx.x, items_per_tile, n_items), lane);
     for (int item = blockIdx.x; active && item < n_items; item += gridDim.x) {
       if (__any_sync(0xffffffffu, *s_abort != 0)) break;  // warp-uniform exit
       const int head = (item % items_per_tile) * hpi + grp;
       const TileRows cur = nxt;
       const int r0 = cur.r0;
-      nxt = tile_rows_load(p, item_r0(p, item + gridDim.x, items_per_tile, n_items), lane);
+      nxt = tile_rows_load<kSeg>(p, item_r0<kSeg>(p, item + gridDim.x, items_per_tile, n_items), lane);
       const RunMasks rm = run_masks(cur, lane);
       const int n_kv = count_tiles(cur, rm, lane);
       const int i = r0 + row;
@@ -733,8 +739,11 @@ pkv_status prefill_paged_entry(const pkv_cache_desc* cache, const void* k_pool,
   static std::atomic<bool> attr_set[64] = {};  // per device; host threads may race to set it
   if (dev < 0 || dev >= 64) return PKV_ERR_DEVICE;
   if (!attr_set[dev].load(std::memory_order_acquire)) {
-    const cudaError_t ea = cudaFuncSetAttribute(
-        prefill_paged_tcgen05_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t ea = cudaFuncSetAttribute(prefill_paged_tcgen05_kernel<false>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (ea == cudaSuccess)
+      ea = cudaFuncSetAttribute(prefill_paged_tcgen05_kernel<true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (ea != cudaSuccess) return record_cuda_status(ea);
     attr_set[dev].store(true, std::memory_order_release);
   }
@@ -768,8 +777,12 @@ pkv_status prefill_paged_entry(const pkv_cache_desc* cache, const void* k_pool,
       prm.seg_start != nullptr ? static_cast<long long>(n_tokens) * (num_q_heads / prm.heads_per_item)
                                : prm.n_items;
   const int grid = items_max < sms ? static_cast<int>(items_max) : sms;
-  const cudaError_t e = launch_kernel(prefill_paged_tcgen05_kernel, dim3(grid), dim3(kThreads),
-                                      kSmemBytes, stream, false, qmap, kmap, vmap, prm);
+  const cudaError_t e =
+      prm.seg_start != nullptr
+          ? launch_kernel(prefill_paged_tcgen05_kernel<true>, dim3(grid), dim3(kThreads),
+                          kSmemBytes, stream, false, qmap, kmap, vmap, prm)
+          : launch_kernel(prefill_paged_tcgen05_kernel<false>, dim3(grid), dim3(kThreads),
+                          kSmemBytes, stream, false, qmap, kmap, vmap, prm);
   return record_cuda_status(e);
 }
 
