@@ -16,8 +16,11 @@
 // of at most 128 tokens, and a tile covers one piece. Fixed 128-token tiles
 // of the packing would straddle runs (decode tokens between chunks shift
 // every later chunk off the 128-token grid) and pay both runs' key ranges.
-// One CTA walks the packing in chunks of 1024 tokens, so both lists are in
-// token order, fixed by the input.
+// One CTA walks the packing, 8 192 tokens a pass (eight consecutive tokens
+// per thread, block-wide scans for the list positions and the run starts),
+// so both lists are in token order, fixed by the input.
+#include <climits>
+
 #include "pkv.h"
 #include "pkv_launch.h"
 
@@ -25,82 +28,137 @@ namespace pkv {
 namespace {
 
 constexpr int kRouteThreads = 1024;
+constexpr int kPer = 8;  // consecutive tokens per thread
 
+// Block-wide exclusive sum of `v` (and the block total) over kRouteThreads
+// threads; `scratch` holds kRouteThreads / 32 ints. Contains __syncthreads.
+__device__ __forceinline__ int block_excl_sum(int v, int* scratch, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = scratch[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    scratch[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  total = scratch[31];
+  const int before = warp > 0 ? scratch[warp - 1] : 0;
+  __syncthreads();  // scratch is reused by the caller's next scan
+  return before + x - v;
+}
+
+// Block-wide exclusive maximum of `v` (identity -1) and the block maximum.
+__device__ __forceinline__ int block_excl_max(int v, int* scratch, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x = max(x, y);
+  }
+  const int up = __shfl_up_sync(0xffffffffu, x, 1);
+  const int in_warp = lane > 0 ? up : -1;
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = scratch[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w = max(w, y);
+    }
+    scratch[lane] = w;
+  }
+  __syncthreads();
+  total = scratch[31];
+  const int before = warp > 0 ? scratch[warp - 1] : -1;
+  __syncthreads();
+  return max(before, in_warp);
+}
+
+// Each thread takes kPer consecutive tokens, so a pass over 8 192 tokens
+// costs one round of loads and four block scans.
 __global__ void __launch_bounds__(kRouteThreads) route_lone_kernel(
     const int32_t* __restrict__ batch_idx, int n_tokens, int cap, int32_t* __restrict__ list,
     int32_t* __restrict__ count, uint8_t* __restrict__ skip, int32_t* __restrict__ seg_start,
     int32_t* __restrict__ seg_count) {
-  __shared__ int s_warp[kRouteThreads / 32];
-  __shared__ int s_wseg[kRouteThreads / 32];
-  __shared__ int s_wmax[kRouteThreads / 32];
-  __shared__ int s_base, s_segbase, s_runstart;
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  const int warp = tid >> 5;
-  constexpr int kWarps = kRouteThreads / 32;
-  if (tid == 0) {
-    s_base = 0;
-    s_segbase = 0;
-    s_runstart = 0;
-  }
-  __syncthreads();
-  for (int c0 = 0; c0 < n_tokens; c0 += kRouteThreads) {
-    const int i = c0 + tid;
-    const bool valid = i < n_tokens;
-    bool run_start = false, lone = false;
-    if (valid) {
-      const int b = batch_idx[i];
-      run_start = i == 0 || batch_idx[i - 1] != b;
-      const bool next_differs = i + 1 == n_tokens || batch_idx[i + 1] != b;
-      lone = b > 0 && run_start && next_differs;
-    }
-    // routed tokens: position among the lone tokens so far
-    const uint32_t bal = __ballot_sync(0xffffffffu, lone);
-    // the latest run start at or before i (prefix max over token indices)
-    int rs = run_start ? i : -1;
+  __shared__ int scratch[kRouteThreads / 32];
+  int base = 0, seg_base = 0, run_carry = -1;  // identical in every thread
+  for (int c0 = 0; c0 < n_tokens; c0 += kRouteThreads * kPer) {
+    const int i0 = c0 + threadIdx.x * kPer;
+    // slots of tokens i0 - 1 .. i0 + kPer; outside the packing they differ
+    // from every slot (run starts and ends there)
+    int b[kPer + 2];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, rs, o);
-      if (lane >= o) rs = max(rs, v);
+    for (int k = 0; k < kPer + 2; ++k) {
+      const int i = i0 - 1 + k;
+      b[k] = (i >= 0 && i < n_tokens) ? __ldg(batch_idx + i) : (i < 0 ? INT_MIN : INT_MIN + 1);
     }
-    if (lane == 0) s_warp[warp] = __popc(bal);
-    if (lane == 31) s_wmax[warp] = rs;
-    __syncthreads();
-    int pos = s_base + __popc(bal & ((1u << lane) - 1u));
-    int rs_in = s_runstart;
-    for (int w = 0; w < warp; ++w) {
-      pos += s_warp[w];
-      rs_in = max(rs_in, s_wmax[w]);
-    }
-    rs = max(rs, rs_in);
-    const bool routed = lone && pos < cap;
-    if (valid) skip[i] = routed ? 1 : 0;
-    if (routed) list[pos] = i;
-    // query tiles of the prefill kernel: run pieces of at most 128 tokens
-    const bool seg = valid && !routed && ((i - rs) & 127) == 0;
-    const uint32_t sbal = __ballot_sync(0xffffffffu, seg);
-    if (lane == 0) s_wseg[warp] = __popc(sbal);
-    __syncthreads();
-    int spos = s_segbase + __popc(sbal & ((1u << lane) - 1u));
-    for (int w = 0; w < warp; ++w) spos += s_wseg[w];
-    if (seg) seg_start[spos] = i;
-    __syncthreads();  // every thread has read the shared counters
-    if (tid == 0) {
-      int tot = 0, stot = 0, mx = s_runstart;
-      for (int w = 0; w < kWarps; ++w) {
-        tot += s_warp[w];
-        stot += s_wseg[w];
-        mx = max(mx, s_wmax[w]);
+    uint32_t lone = 0, start = 0;
+    int last_start = -1;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = i0 + k;
+      if (i >= n_tokens) break;
+      const bool st = b[k] != b[k + 1];
+      if (st) {
+        start |= 1u << k;
+        last_start = i;
       }
-      s_base += tot;
-      s_segbase += stot;
-      s_runstart = mx;
+      if (b[k + 1] > 0 && st && b[k + 2] != b[k + 1]) lone |= 1u << k;
     }
-    __syncthreads();
+    int lone_total, max_total;
+    const int lone_before = block_excl_sum(__popc(lone), scratch, lone_total);
+    // the run in force at each token: the last run start at or before it,
+    // earlier threads' and earlier passes' starts included
+    const int prev = max(run_carry, block_excl_max(last_start, scratch, max_total));
+    int rs_tok[kPer];
+    {
+      int cur = prev;
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        if ((start >> k) & 1u) cur = i0 + k;
+        rs_tok[k] = cur;
+      }
+    }
+    uint32_t seg = 0;
+    int pos = base + lone_before;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = i0 + k;
+      if (i >= n_tokens) break;
+      bool routed = false;
+      if ((lone >> k) & 1u) {
+        routed = pos < cap;
+        if (routed) list[pos] = i;
+        ++pos;
+      }
+      skip[i] = routed ? 1 : 0;
+      if (!routed && ((i - rs_tok[k]) & 127) == 0) seg |= 1u << k;
+    }
+    int seg_total;
+    int spos = seg_base + block_excl_sum(__popc(seg), scratch, seg_total);
+#pragma unroll
+    for (int k = 0; k < kPer; ++k)
+      if ((seg >> k) & 1u) seg_start[spos++] = i0 + k;
+    base += lone_total;
+    seg_base += seg_total;
+    run_carry = max(run_carry, max_total);
   }
-  if (tid == 0) {
-    *count = min(s_base, cap);
-    *seg_count = s_segbase;
+  if (threadIdx.x == 0) {
+    *count = min(base, cap);
+    *seg_count = seg_base;
   }
 }
 
