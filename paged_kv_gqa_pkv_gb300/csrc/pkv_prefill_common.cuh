@@ -2,7 +2,8 @@
 // sizes, the tensor-memory layout, the MMA instruction descriptors, the
 // softmax row (P into shared memory for the packed kernel, into tensor memory
 // for the paged one), the bounded wait that honours a grid-wide abort flag,
-// and the host-side cuTensorMapEncodeTiled lookup. Each kernel file lays out
+// the cost-sorted item schedule, and the host-side cuTensorMapEncodeTiled
+// lookup. Each kernel file lays out
 // its own shared memory.
 #pragma once
 
@@ -310,6 +311,142 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
       }
     }
   }
+}
+
+// ---------------------------------------------------------------------------
+// Item schedule of the persistent paged-prefill grid. An item is (query tile,
+// head group); its cost is mostly its number of key tiles, which varies
+// several-fold across the tiles of a step (a chunk over a 4 K prefix against
+// one over 512 keys). Dealt round-robin, the busiest CTA of 16 chunks of 512
+// tokens over prefixes U[512, 4096] carries 1.27x the mean load. Sorting
+// tiles by cost alone brings that to 1.02x but scatters the tiles of one
+// sequence, which share its K/V in L2, over the whole call (the mean CTA time
+// grew 7 %). So tiles are grouped: consecutive tiles that continue one run of
+// equal slots form a group, groups are sorted by their largest tile cost,
+// largest first (a stable counting sort, identical in every CTA), and a
+// group's tiles follow each other, last (costliest) tile first. The items in
+// that order (a tile's head groups side by side) are dealt in snake order:
+// round r gives position r*G + b to CTA b, reversed in odd rounds. The
+// estimate only orders the work; which CTA computes an item changes nothing
+// in its result. Calls with more than kSchedMaxTiles query tiles are dealt
+// round-robin.
+constexpr int kSchedMaxTiles = 768;
+constexpr int kSchedListMax = 768;                 // this CTA's items + end mark
+constexpr int kSchedBytes = kSchedListMax * 2;     // uint16 item list
+constexpr int kSchedMaxCost = 255;
+constexpr uint16_t kSchedEnd = 0xFFFFu;
+// transient scratch (in the K/V ring, before any load): 256 bins, per tile
+// its cost, its link to the next tile and its group's sort key, then the
+// tile order
+constexpr int kSchedScratchBytes = 1024 + 3 * kSchedMaxTiles + 2 * kSchedMaxTiles;
+
+// listed: this CTA's items are list[0..] up to kSchedEnd; else round-robin
+struct ItemSched {
+  bool listed;
+  int n_items;
+};
+
+// This CTA's r-th item (r = 0, 1, ... up to one past its last), or -1.
+__device__ __forceinline__ int sched_item(const ItemSched& s, const uint16_t* list, int r) {
+  if (s.listed) {
+    const uint16_t v = list[r];
+    return v == kSchedEnd ? -1 : static_cast<int>(v);
+  }
+  const long long it = static_cast<long long>(r) * gridDim.x + blockIdx.x;
+  return it < s.n_items ? static_cast<int>(it) : -1;
+}
+
+// Called by every thread of the CTA (it holds block barriers). cost(t) is the
+// estimated cost of tile t (clamped to [0, kSchedMaxCost]); link(t) says that
+// tile t + 1 continues tile t's last run (t + 1 < n_tiles). scratch holds
+// kSchedScratchBytes that nothing else uses until this returns; list gets
+// this CTA's items.
+template <class CostFn, class LinkFn>
+__device__ ItemSched sched_build(uint16_t* list, uint8_t* scratch, int n_tiles,
+                                 int items_per_tile, CostFn cost, LinkFn link) {
+  ItemSched s;
+  s.listed = false;
+  s.n_items = n_tiles * items_per_tile;
+  const int g = static_cast<int>(gridDim.x);
+  if (n_tiles <= 1 || n_tiles > kSchedMaxTiles || s.n_items >= kSchedEnd ||
+      (s.n_items + g - 1) / g >= kSchedListMax)
+    return s;
+  int* hist = reinterpret_cast<int*>(scratch);     // [256], bin = kSchedMaxCost - key
+  uint8_t* tcost = scratch + 1024;                 // [n_tiles]
+  uint8_t* tlink = tcost + kSchedMaxTiles;         // [n_tiles]
+  uint8_t* bin = tlink + kSchedMaxTiles;           // [n_tiles]
+  uint16_t* order = reinterpret_cast<uint16_t*>(bin + kSchedMaxTiles);  // [n_tiles]
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+  for (int t = threadIdx.x; t < n_tiles; t += blockDim.x) {
+    tcost[t] = static_cast<uint8_t>(min(max(cost(t), 0), kSchedMaxCost));
+    tlink[t] = (t + 1 < n_tiles && link(t)) ? 1 : 0;
+  }
+  __syncthreads();
+  // the first tile of each group finds the group's largest cost and gives
+  // every tile of the group that key
+  for (int t = threadIdx.x; t < n_tiles; t += blockDim.x) {
+    if (t > 0 && tlink[t - 1]) continue;
+    int e = t, mx = tcost[t];
+    while (tlink[e]) mx = max(mx, static_cast<int>(tcost[++e]));
+    for (int u = t; u <= e; ++u) bin[u] = static_cast<uint8_t>(kSchedMaxCost - mx);
+    atomicAdd(&hist[kSchedMaxCost - mx], e - t + 1);
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    // exclusive scan of the bins: each lane holds eight consecutive bins
+    int v[8], sum = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      v[k] = hist[8 * lane + k];
+      sum += v[k];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      hist[8 * lane + k] = run;
+      run += v[k];
+    }
+    __syncwarp();
+    // stable placement, 32 tiles a pass from the last tile down: lanes with
+    // equal keys take consecutive places after the bin's running offset
+    for (int c0 = 0; c0 < n_tiles; c0 += 32) {
+      const int t = n_tiles - 1 - (c0 + lane);
+      const bool valid = t >= 0;
+      const int k = valid ? static_cast<int>(bin[t]) : 256 + lane;
+      const uint32_t peers = __match_any_sync(0xffffffffu, k);
+      const int leader = __ffs(peers) - 1;
+      int base = (valid && lane == leader) ? hist[k] : 0;
+      base = __shfl_sync(0xffffffffu, base, leader);
+      if (valid) order[base + __popc(peers & ((1u << lane) - 1u))] = static_cast<uint16_t>(t);
+      __syncwarp();
+      if (valid && lane == leader) hist[k] = base + __popc(peers);
+      __syncwarp();
+    }
+    // this CTA's items: position r*G + b of the ordered items in even rounds,
+    // r*G + G-1-b in odd ones, then the end mark
+    const int b = static_cast<int>(blockIdx.x);
+    for (int r = lane; r < kSchedListMax; r += 32) {
+      const long long pos = static_cast<long long>(r) * g + ((r & 1) ? g - 1 - b : b);
+      uint16_t v = kSchedEnd;
+      if (pos < s.n_items) {
+        const int ps = static_cast<int>(pos);
+        v = static_cast<uint16_t>(static_cast<int>(order[ps / items_per_tile]) * items_per_tile +
+                                  ps % items_per_tile);
+      }
+      list[r] = v;
+      if (__all_sync(0xffffffffu, v == kSchedEnd)) break;
+    }
+  }
+  __syncthreads();
+  s.listed = true;
+  return s;
 }
 
 }  // namespace prefill_detail

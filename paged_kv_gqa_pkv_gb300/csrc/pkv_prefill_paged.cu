@@ -12,7 +12,8 @@
 //
 // The kernel keeps the packed prefill's roles (pkv_prefill.cu): a persistent
 // grid walks items of one 128-row query tile x two query heads of a GQA
-// group; warp 0 loads Q and a 5-slot ring of 128-key K/V tiles by TMA, warp 1
+// group, dealt by estimated cost, largest first, a sequence's tiles together
+// (sched_build in pkv_prefill_common.cuh); warp 0 loads Q and a 5-slot ring of 128-key K/V tiles by TMA, warp 1
 // issues the tcgen05 MMAs, warps 2..9 run the masked online softmax, one row
 // per thread, and the epilogue. Two things differ in the tile loop:
 //  * P stays in tensor memory: the softmax writes it as bf16 pairs over the
@@ -63,7 +64,9 @@ constexpr int kOffBar = kOffRing + kRing * kTileBytes;
 // pv_done[2], o_free[2]
 constexpr int kNumBars = 2 + 2 * kRing + 8;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;      // tmem slot, abort flag
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;      // + slack for 1024 alignment
+constexpr int kOffSched = kOffMisc + 16;              // this CTA's item list
+constexpr int kSmemBytes = kOffSched + kSchedBytes + 1024;  // + slack for 1024 alignment
+static_assert(kRing * kTileBytes >= kSchedScratchBytes, "schedule scratch lives in the ring");
 static_assert(kSmemBytes <= kMaxDynSmem, "shared memory above the opt-in limit");
 
 struct PagedPrefillParams {
@@ -249,7 +252,7 @@ __device__ __forceinline__ int call_items(const PagedPrefillParams& p, int items
 template <bool kSeg>
 __device__ __forceinline__ int item_r0(const PagedPrefillParams& p, int item, int items_per_tile,
                                        int n_items) {
-  if (item >= n_items) return -1;
+  if (item < 0 || item >= n_items) return -1;
   const int tile = item / items_per_tile;
   return kSeg ? __ldg(p.seg_start + tile) : tile * kBM;
 }
@@ -285,6 +288,7 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
   const int lane = threadIdx.x & 31;
   const int hpi = p.heads_per_item;
   const int items_per_tile = p.num_q_heads / hpi;
+  const int n_tiles = kSeg ? *p.seg_count : p.n_tiles;
   const int n_items = call_items<kSeg>(p, items_per_tile);
 
   if (threadIdx.x == 0) {
@@ -313,6 +317,28 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // tile cost: key tiles of the run at the tile's first row, plus those of
+  // the run at its last row when that is another run of a fixed window, plus
+  // one for the item's Q load and epilogue
+  const uint16_t* s_list = reinterpret_cast<const uint16_t*>(smem + kOffSched);
+  const ItemSched S = sched_build(
+      reinterpret_cast<uint16_t*>(smem + kOffSched), smem + kOffRing, n_tiles, items_per_tile,
+      [&](int t) -> int {
+        const int r0 = kSeg ? __ldg(p.seg_start + t) : t * kBM;
+        if (r0 < 0 || r0 >= p.n_tokens) return 0;
+        const int rl = min(r0 + kBM, p.n_tokens) - 1;
+        const int b0 = __ldg(p.batch_idx + r0), bl = __ldg(p.batch_idx + rl);
+        const int q0 = __ldg(p.input_pos + r0), ql = __ldg(p.input_pos + rl);
+        auto tiles = [](int b, int pos) { return (b != 0 && pos >= 0) ? pos / kBN + 1 : 0; };
+        if (b0 == bl) return tiles(b0, max(q0, ql)) + 1;
+        return tiles(b0, q0) + (kSeg ? 0 : tiles(bl, ql)) + 1;
+      },
+      [&](int t) -> bool {  // the next tile's first row is in this tile's last run
+        const int r1 = kSeg ? __ldg(p.seg_start + t + 1) : (t + 1) * kBM;
+        if (r1 <= 0 || r1 >= p.n_tokens) return false;
+        const int b1 = __ldg(p.batch_idx + r1);
+        return b1 != 0 && b1 == __ldg(p.batch_idx + r1 - 1);
+      });
 
   if (warp == 0) {
     // ---------------------------------------------------- TMA producer ----
@@ -320,13 +346,14 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
     uint32_t qi = 0;  // non-empty items
     const int R = p.box_rows;
     const int nsub = kBN / R;  // boxes per head-dim half of a key tile (1..8)
-    TileRows nxt = tile_rows_load<kSeg>(p, item_r0<kSeg>(p, blockIdx.x, items_per_tile, n_items), lane);
-    for (int item = blockIdx.x; item < n_items && !*s_abort; item += gridDim.x) {
+    int item = sched_item(S, s_list, 0);
+    TileRows nxt = tile_rows_load<kSeg>(p, item_r0<kSeg>(p, item, items_per_tile, n_items), lane);
+    for (int r = 0; item >= 0 && !*s_abort; item = sched_item(S, s_list, ++r)) {
       const int h0 = (item % items_per_tile) * hpi;
       const int kvh = h0 / p.group;
       const TileRows cur = nxt;
       const int r0 = cur.r0;
-      nxt = tile_rows_load<kSeg>(p, item_r0<kSeg>(p, item + gridDim.x, items_per_tile, n_items), lane);
+      nxt = tile_rows_load<kSeg>(p, item_r0<kSeg>(p, sched_item(S, s_list, r + 1), items_per_tile, n_items), lane);
       const RunMasks rm = run_masks(cur, lane);
       const int n_kv = count_tiles(cur, rm, lane);
       if (n_kv == 0) continue;
@@ -440,10 +467,11 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
       if (elect_one()) umma_commit(bar);
       __syncwarp();
     };
-    TileRows nxt = tile_rows_load<kSeg>(p, item_r0<kSeg>(p, blockIdx.x, items_per_tile, n_items), lane);
-    for (int item = blockIdx.x; item < n_items && !*s_abort; item += gridDim.x) {
+    int item = sched_item(S, s_list, 0);
+    TileRows nxt = tile_rows_load<kSeg>(p, item_r0<kSeg>(p, item, items_per_tile, n_items), lane);
+    for (int r = 0; item >= 0 && !*s_abort; item = sched_item(S, s_list, ++r)) {
       const TileRows cur = nxt;
-      nxt = tile_rows_load<kSeg>(p, item_r0<kSeg>(p, item + gridDim.x, items_per_tile, n_items), lane);
+      nxt = tile_rows_load<kSeg>(p, item_r0<kSeg>(p, sched_item(S, s_list, r + 1), items_per_tile, n_items), lane);
       const RunMasks rm = run_masks(cur, lane);
       const int n_kv = count_tiles(cur, rm, lane);
       if (n_kv == 0) continue;
@@ -533,13 +561,14 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
     const uint32_t t_o = tmem + (static_cast<uint32_t>(lane_base) << 16) + 256 + grp * kHeadDim;
     uint32_t tc = 0, qi = 0;
     const bool active = grp < hpi;
-    TileRows nxt = tile_rows_load<kSeg>(p, item_r0<kSeg>(p, blockIdx.x, items_per_tile, n_items), lane);
-    for (int item = blockIdx.x; active && item < n_items; item += gridDim.x) {
+    int item = sched_item(S, s_list, 0);
+    TileRows nxt = tile_rows_load<kSeg>(p, item_r0<kSeg>(p, item, items_per_tile, n_items), lane);
+    for (int r = 0; active && item >= 0; item = sched_item(S, s_list, ++r)) {
       if (__any_sync(0xffffffffu, *s_abort != 0)) break;  // warp-uniform exit
       const int head = (item % items_per_tile) * hpi + grp;
       const TileRows cur = nxt;
       const int r0 = cur.r0;
-      nxt = tile_rows_load<kSeg>(p, item_r0<kSeg>(p, item + gridDim.x, items_per_tile, n_items), lane);
+      nxt = tile_rows_load<kSeg>(p, item_r0<kSeg>(p, sched_item(S, s_list, r + 1), items_per_tile, n_items), lane);
       const RunMasks rm = run_masks(cur, lane);
       const int n_kv = count_tiles(cur, rm, lane);
       const int i = r0 + row;
