@@ -11,9 +11,10 @@
 // numbered 0, 1, 2, ...; then the keys of query i are exactly the packed rows
 // [i - input_pos[i], i]. A row that breaks it sets PKV_DEV_ERR_LAYOUT.
 //
-// Schedule: a persistent grid (one CTA per SM) walks the work items
-// round-robin; an item is one 128-row query tile for TWO query heads of the
-// same GQA group, so every K/V tile is loaded once for both heads (a group of
+// Schedule: a persistent grid (one CTA per SM) walks the work items, sorted
+// by estimated cost within windows of eight rounds and dealt in snake order
+// (sched_build_windowed in pkv_prefill_common.cuh); an item is one 128-row
+// query tile for TWO query heads of the same GQA group, so every K/V tile is loaded once for both heads (a group of
 // one head, G == 1, gives one-head items). Warp roles:
 //  * warp 0 issues TMA: each item's Q tiles, then K and V tiles of 128 keys
 //    into a 3-slot ring of 32 KB half-stages, in the MMA thread's order
@@ -55,7 +56,9 @@ constexpr int kOffBar = kOffRing + kRing * kTileBytes;
 // pv_done[2], o_free[2], s_free[2], grp_sync[2]
 constexpr int kNumBars = 20;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;      // tmem slot, abort flag
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;      // + slack for 1024 alignment
+constexpr int kOffSched = kOffMisc + 16;              // this CTA's item list
+constexpr int kSmemBytes = kOffSched + kSchedBytes + 1024;  // + slack for 1024 alignment
+static_assert(kRing * kTileBytes >= kSchedScratchBytes, "schedule scratch lives in the ring");
 static_assert(kSmemBytes <= kMaxDynSmem, "shared memory above the opt-in limit");
 
 struct PrefillParams {
@@ -134,7 +137,7 @@ __device__ __forceinline__ RowRaw row_raw_load(const PrefillParams& p, int i) {
 }
 
 __device__ __forceinline__ int item_r0(const PrefillParams& p, int item, int items_per_tile) {
-  return item < p.n_items ? (item / items_per_tile) * kBM : -1;
+  return (item >= 0 && item < p.n_items) ? (item / items_per_tile) * kBM : -1;
 }
 
 }  // namespace
@@ -199,20 +202,34 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // tile cost: key tiles from the first row's document start to the last row
+  // (the packing precondition), plus one for the item's Q load and epilogue
+  const uint16_t* s_list = reinterpret_cast<const uint16_t*>(smem + kOffSched);
+  const ItemSched S = sched_build_windowed(
+      reinterpret_cast<uint16_t*>(smem + kOffSched), smem + kOffRing, p.n_tiles, items_per_tile,
+      (8 * static_cast<int>(gridDim.x)) / items_per_tile, [&](int t) -> int {
+        const int r0 = t * kBM;
+        const int rl = min(r0 + kBM, p.n_tokens) - 1;
+        const int b0 = __ldg(p.batch_idx + r0);
+        const int p0 = __ldg(p.input_pos + r0);
+        const int lo = (b0 != 0 && p0 >= 0 && p0 <= r0) ? r0 - p0 : r0;
+        return (rl + 1 - lo + kBN - 1) / kBN + 1;
+      });
 
   if (warp == 0) {
     // ---------------------------------------------------- TMA producer ----
     uint32_t L = 0;   // ring loads issued
     uint32_t qi = 0;  // non-empty items
-    TileRaw raw = tile_raw_load(p, item_r0(p, blockIdx.x, items_per_tile), lane);
-    for (int item = blockIdx.x; item < p.n_items && !*s_abort; item += gridDim.x) {
+    int item = sched_item(S, s_list, 0);
+    TileRaw raw = tile_raw_load(p, item_r0(p, item, items_per_tile), lane);
+    for (int r = 0; item >= 0 && !*s_abort; item = sched_item(S, s_list, ++r)) {
       const int tile = item / items_per_tile;
       const int h0 = (item % items_per_tile) * hpi;
       const int kvh = h0 / p.group;
       const int r0 = tile * kBM;
       int kv_lo, kv_hi;
       tile_key_range(raw, r0, lane, kv_lo, kv_hi);
-      raw = tile_raw_load(p, item_r0(p, item + gridDim.x, items_per_tile), lane);
+      raw = tile_raw_load(p, item_r0(p, sched_item(S, s_list, r + 1), items_per_tile), lane);
       if (kv_hi <= kv_lo) continue;
       const int n_kv = (kv_hi - kv_lo + kBN - 1) / kBN;
       if (lane == 0) {
@@ -310,12 +327,13 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
       }
       __syncwarp();
     };
-    TileRaw raw = tile_raw_load(p, item_r0(p, blockIdx.x, items_per_tile), lane);
-    for (int item = blockIdx.x; item < p.n_items && !*s_abort; item += gridDim.x) {
+    int item = sched_item(S, s_list, 0);
+    TileRaw raw = tile_raw_load(p, item_r0(p, item, items_per_tile), lane);
+    for (int r = 0; item >= 0 && !*s_abort; item = sched_item(S, s_list, ++r)) {
       const int r0 = (item / items_per_tile) * kBM;
       int kv_lo, kv_hi;
       tile_key_range(raw, r0, lane, kv_lo, kv_hi);
-      raw = tile_raw_load(p, item_r0(p, item + gridDim.x, items_per_tile), lane);
+      raw = tile_raw_load(p, item_r0(p, sched_item(S, s_list, r + 1), items_per_tile), lane);
       if (kv_hi <= kv_lo) continue;
       const int n_kv = (kv_hi - kv_lo + kBN - 1) / kBN;
       // K_0: S_h must have been read by the softmax of the previous tile
@@ -371,10 +389,11 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
       return __all_sync(0xffffffffu, w);
     };
     const bool active = grp < hpi;
-    TileRaw raw = tile_raw_load(p, item_r0(p, blockIdx.x, items_per_tile), lane);
-    const int r0_first = item_r0(p, blockIdx.x, items_per_tile);
+    int item = sched_item(S, s_list, 0);
+    TileRaw raw = tile_raw_load(p, item_r0(p, item, items_per_tile), lane);
+    const int r0_first = item_r0(p, item, items_per_tile);
     RowRaw rr = row_raw_load(p, r0_first >= 0 ? r0_first + row : -1);
-    for (int item = blockIdx.x; active && item < p.n_items; item += gridDim.x) {
+    for (int r = 0; active && item >= 0; item = sched_item(S, s_list, ++r)) {
       if (__any_sync(0xffffffffu, *s_abort != 0)) break;  // warp-uniform exit
       const int tile = item / items_per_tile;
       const int head = (item % items_per_tile) * hpi + grp;
@@ -394,7 +413,7 @@ prefill_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
       }
       // next item's metadata, in flight while this item computes
       {
-        const int r0n = item_r0(p, item + gridDim.x, items_per_tile);
+        const int r0n = item_r0(p, sched_item(S, s_list, r + 1), items_per_tile);
         raw = tile_raw_load(p, r0n, lane);
         rr = row_raw_load(p, r0n >= 0 ? r0n + row : -1);
       }

@@ -356,6 +356,34 @@ __device__ __forceinline__ int sched_item(const ItemSched& s, const uint16_t* li
   return it < s.n_items ? static_cast<int>(it) : -1;
 }
 
+// A sorted schedule needs at most kSchedMaxTiles tiles and item indices
+// below the end mark, and this CTA's list must fit.
+__device__ __forceinline__ bool sched_fits(int n_tiles, int n_items) {
+  const int g = static_cast<int>(gridDim.x);
+  return n_tiles > 1 && n_tiles <= kSchedMaxTiles && n_items < kSchedEnd &&
+         (n_items + g - 1) / g < kSchedListMax;
+}
+
+// Warp 0: this CTA's items (position r*G + b of the ordered items in even
+// rounds, r*G + G-1-b in odd ones, a tile's head groups side by side), then
+// the end mark.
+__device__ __forceinline__ void sched_fill_list(uint16_t* list, const uint16_t* order,
+                                                int n_items, int items_per_tile, int lane) {
+  const int g = static_cast<int>(gridDim.x);
+  const int b = static_cast<int>(blockIdx.x);
+  for (int r = lane; r < kSchedListMax; r += 32) {
+    const long long pos = static_cast<long long>(r) * g + ((r & 1) ? g - 1 - b : b);
+    uint16_t v = kSchedEnd;
+    if (pos < n_items) {
+      const int ps = static_cast<int>(pos);
+      v = static_cast<uint16_t>(static_cast<int>(order[ps / items_per_tile]) * items_per_tile +
+                                ps % items_per_tile);
+    }
+    list[r] = v;
+    if (__all_sync(0xffffffffu, v == kSchedEnd)) break;
+  }
+}
+
 // Called by every thread of the CTA (it holds block barriers). cost(t) is the
 // estimated cost of tile t (clamped to [0, kSchedMaxCost]); link(t) says that
 // tile t + 1 continues tile t's last run (t + 1 < n_tiles). scratch holds
@@ -367,10 +395,7 @@ __device__ ItemSched sched_build(uint16_t* list, uint8_t* scratch, int n_tiles,
   ItemSched s;
   s.listed = false;
   s.n_items = n_tiles * items_per_tile;
-  const int g = static_cast<int>(gridDim.x);
-  if (n_tiles <= 1 || n_tiles > kSchedMaxTiles || s.n_items >= kSchedEnd ||
-      (s.n_items + g - 1) / g >= kSchedListMax)
-    return s;
+  if (!sched_fits(n_tiles, s.n_items)) return s;
   int* hist = reinterpret_cast<int*>(scratch);     // [256], bin = kSchedMaxCost - key
   uint8_t* tcost = scratch + 1024;                 // [n_tiles]
   uint8_t* tlink = tcost + kSchedMaxTiles;         // [n_tiles]
@@ -429,21 +454,45 @@ __device__ ItemSched sched_build(uint16_t* list, uint8_t* scratch, int n_tiles,
       if (valid && lane == leader) hist[k] = base + __popc(peers);
       __syncwarp();
     }
-    // this CTA's items: position r*G + b of the ordered items in even rounds,
-    // r*G + G-1-b in odd ones, then the end mark
-    const int b = static_cast<int>(blockIdx.x);
-    for (int r = lane; r < kSchedListMax; r += 32) {
-      const long long pos = static_cast<long long>(r) * g + ((r & 1) ? g - 1 - b : b);
-      uint16_t v = kSchedEnd;
-      if (pos < s.n_items) {
-        const int ps = static_cast<int>(pos);
-        v = static_cast<uint16_t>(static_cast<int>(order[ps / items_per_tile]) * items_per_tile +
-                                  ps % items_per_tile);
-      }
-      list[r] = v;
-      if (__all_sync(0xffffffffu, v == kSchedEnd)) break;
-    }
+    sched_fill_list(list, order, s.n_items, items_per_tile, lane);
   }
+  __syncthreads();
+  s.listed = true;
+  return s;
+}
+
+// Packed documents: the tiles of one document are spread over the packing's
+// order, and tiles that share a document's K/V run close together when the
+// order is kept; sorting all tiles by cost scatters them (the mean CTA time
+// grew 10 %). Here the tiles are sorted by cost within consecutive windows of
+// `window` tiles (eight rounds of items), so each window's K/V stays in L2
+// while its items are balanced. O(n_tiles * window) comparisons in all.
+template <class CostFn>
+__device__ ItemSched sched_build_windowed(uint16_t* list, uint8_t* scratch, int n_tiles,
+                                          int items_per_tile, int window, CostFn cost) {
+  ItemSched s;
+  s.listed = false;
+  s.n_items = n_tiles * items_per_tile;
+  if (!sched_fits(n_tiles, s.n_items) || window < 2) return s;
+  uint8_t* tcost = scratch;                                              // [n_tiles]
+  uint16_t* order = reinterpret_cast<uint16_t*>(scratch + kSchedMaxTiles);  // [n_tiles]
+  for (int t = threadIdx.x; t < n_tiles; t += blockDim.x)
+    tcost[t] = static_cast<uint8_t>(min(max(cost(t), 0), kSchedMaxCost));
+  __syncthreads();
+  // rank within the window: larger cost first, ties in tile order
+  for (int t = threadIdx.x; t < n_tiles; t += blockDim.x) {
+    const int w0 = (t / window) * window;
+    const int w1 = min(w0 + window, n_tiles);
+    const int c = tcost[t];
+    int rank = w0;
+    for (int u = w0; u < w1; ++u) {
+      const int cu = tcost[u];
+      rank += (cu > c || (cu == c && u < t)) ? 1 : 0;
+    }
+    order[rank] = static_cast<uint16_t>(t);
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) sched_fill_list(list, order, s.n_items, items_per_tile, threadIdx.x);
   __syncthreads();
   s.listed = true;
   return s;
