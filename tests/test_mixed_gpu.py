@@ -157,3 +157,24 @@ def test_workspace_checked_and_reused_across_calls():
     ref_o, ref_l, _, bad = oracle_mixed(c)
     assert not bad
     assert_attention_close(o1.cpu(), l1.cpu(), ref_o, ref_l)
+
+
+def test_more_than_768_query_tiles_round_robin():
+    """200 chunks of 512 tokens and 30 decode tokens: 800 listed query tiles,
+    past the sorted schedule's limit, so the prefill kernel deals them
+    round-robin; sampled tokens (every decode token, the ends of every chunk
+    and 400 others) against the oracle."""
+    c = W.chunked_prefill(14, n_chunks=200, chunk=512, prefix_lo=0, prefix_hi=256, n_decode=30,
+                          decode_lo=1, decode_hi=600, hq=8, hkv=2)
+    _, _, out, lse, err = run_mixed(c)
+    assert err == 0
+    b = c.batch_idx.numpy()
+    edges = np.flatnonzero(np.diff(b))
+    rows = {0, len(b) - 1}
+    rows.update(edges.tolist())
+    rows.update((edges + 1).tolist())
+    rows.update(np.random.default_rng(14).choice(len(b), 400, replace=False).tolist())
+    rows = sorted(rows)
+    ro, rl, bad_tok, bad = oracle_mixed(c, rows=rows)
+    assert not bad_tok and not bad
+    assert_attention_close(out, lse, ro, rl, rows=rows, tag="mixed 800 tiles")

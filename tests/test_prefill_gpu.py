@@ -125,3 +125,37 @@ def test_prefill_rejects_bad_host_arguments():
         binding.pkv_prefill_attention(gpu(c.q), gpu(c.k), gpu(c.v), gpu(c.batch_idx),
                                       gpu(c.input_pos), -0.1)
     assert e.value.status == 1
+
+
+def _sampled_rows(case, n_random, seed):
+    """Every document's first and last rows and n_random others."""
+    rows = set()
+    start = 0
+    for n in case.doc_lens:
+        rows.update((start, start + n - 1))
+        start += n
+    rng = np.random.default_rng(seed)
+    rows.update(rng.choice(case.n_tokens, n_random, replace=False).tolist())
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("n_tiles", [330, 768, 769])
+def test_item_schedule_sorted_windows_and_round_robin(n_tiles):
+    """The items are sorted by estimated cost within windows of eight rounds
+    (here 304 query tiles: one head pair per item, 152 SMs) up to 768 query
+    tiles and dealt round-robin above: a last window cut short (330), the
+    limit (768) and one tile past it (769). Documents of U[64, 1200] tokens;
+    every document's first and last rows and 400 others against the oracle."""
+    T = n_tiles * 128 - 37
+    rng = np.random.default_rng(n_tiles)
+    lens = []
+    while sum(lens) < T:
+        lens.append(int(rng.integers(64, 1201)))
+    lens[-1] = T - sum(lens[:-1])
+    c = W.packed_prefill(9, doc_lens=lens, hq=8, hkv=2)
+    assert c.n_tokens == T and (T + 127) // 128 == n_tiles
+    out, lse, err = _run(c)
+    assert err == 0
+    rows = _sampled_rows(c, 400, n_tiles)
+    ro, rl = _oracle(c, rows=rows)
+    assert_attention_close(out, lse, ro, rl, rows=rows, tag=f"{n_tiles} tiles")

@@ -177,3 +177,43 @@ def test_output_alignment_paths(offset_elems):
     # nothing written outside out
     rest = torch.cat([buf[:offset_elems], buf[offset_elems + T * hq * d:]]).cpu()
     assert torch.isnan(rest.float()).all()
+
+
+def _sampled_tokens(c, n_random, seed):
+    """First and last token of every run of one slot, and n_random others."""
+    b = c.batch_idx.numpy()
+    edges = np.flatnonzero(np.diff(b)) if len(b) > 1 else np.zeros(0, dtype=np.int64)
+    rows = {0, len(b) - 1}
+    rows.update(edges.tolist())
+    rows.update((edges + 1).tolist())
+    rng = np.random.default_rng(seed)
+    rows.update(rng.choice(len(b), min(n_random, len(b)), replace=False).tolist())
+    return sorted(rows)
+
+
+def test_item_schedule_groups_of_many_tiles():
+    """Items are dealt by estimated cost with the tiles of one run of equal
+    slots kept together, costliest first: runs of 32, 6, 2 and 1 query tiles
+    and a run of two tokens, shuffled, page 64."""
+    c = W.chunked_prefill(12, prefix_lens=[100, 3000, 0, 50, 700, 9],
+                          chunk_lens=[4096, 700, 129, 2, 300, 1], hq=8, hkv=2, page_size=64)
+    _, _, out, lse, err = run_chunked(c)
+    assert err == 0
+    rows = _sampled_tokens(c, 600, 12)
+    ro, rl, bad_tok, bad = oracle_chunked(c, rows=rows)
+    assert not bad_tok and not bad
+    assert_attention_close(out, lse, ro, rl, rows=rows, tag="groups")
+
+
+def test_item_schedule_round_robin_above_768_tiles():
+    """200 chunks of 512 tokens (800 query tiles) over prefixes U[0, 256]:
+    past the sorted schedule's 768 tiles the items are dealt round-robin."""
+    c = W.chunked_prefill(13, n_chunks=200, chunk=512, prefix_lo=0, prefix_hi=256, n_decode=0,
+                          hq=8, hkv=2)
+    assert (c.n_tokens + 127) // 128 == 800
+    _, _, out, lse, err = run_chunked(c)
+    assert err == 0
+    rows = _sampled_tokens(c, 400, 13)
+    ro, rl, bad_tok, bad = oracle_chunked(c, rows=rows)
+    assert not bad_tok and not bad
+    assert_attention_close(out, lse, ro, rl, rows=rows, tag="800 tiles")
