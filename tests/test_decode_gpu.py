@@ -224,3 +224,57 @@ def test_page_sizes_that_are_not_powers_of_two_or_above_a_tile_row(ps, permute):
     lens = [1, 15, 16, 17, ps - 1, ps, ps + 1, 2 * ps + 16, 3 * ps + 5, 700]
     c = W.custom_decode(31, lens, hq=32, hkv=8, page_size=ps, permute=permute)
     _full_parity(c)
+
+
+@pytest.mark.parametrize("fill", ["random", "ones", "zeros"])
+def test_workspace_needs_no_initialisation(fill):
+    """The decode workspace's contents need no initialisation: whatever bits
+    it starts with, and however often it is reused (eager calls, and replays
+    of captured back-to-back calls), every call matches the oracle and every
+    result is bit-identical to the first."""
+    c = W.qwen3_b64_decode(3, permute=True)
+    kp, vp, table = gpu(c.k_pool), gpu(c.v_pool), gpu(c.page_table)
+    q, bi, sl = gpu(c.q), gpu(c.batch_idx), gpu(c.seq_lens)
+    need = binding.pkv_decode_workspace_size(kp, table, c.page_size, c.batch, c.num_q_heads)
+    if fill == "random":
+        g = torch.Generator(device="cuda").manual_seed(9)
+        ws = torch.randint(0, 256, (need,), dtype=torch.uint8, device="cuda", generator=g)
+    else:
+        ws = torch.full((need,), 0xFF if fill == "ones" else 0, dtype=torch.uint8, device="cuda")
+    err = new_dev_err()
+    out = torch.empty((c.batch, c.num_q_heads, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((c.batch, c.num_q_heads), dtype=torch.float32, device="cuda")
+
+    def call():
+        binding.pkv_decode_attention(kp, vp, table, q, bi, sl, c.page_size, c.scale, out=out,
+                                     lse=lse, workspace=ws, dev_err=err)
+
+    _, _, ref_o, ref_l, _, _ = oracle_decode_step(c, append=False)
+    call()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_attention_close(out.cpu(), lse.cpu(), ref_o, ref_l, tag=f"{c.name}-{fill}")
+    o0, l0 = out.clone(), lse.clone()
+    for _ in range(2):  # eager calls on the same workspace
+        out.zero_()
+        call()
+        torch.cuda.synchronize()
+        assert torch.equal(out, o0) and torch.equal(lse, l0)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        call()
+        s.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=s):
+            for _ in range(3):  # back-to-back calls on one workspace
+                call()
+    torch.cuda.synchronize()
+    for _ in range(3):  # replays of the captured calls
+        out.zero_()
+        lse.zero_()
+        gr.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, o0) and torch.equal(lse, l0)
+    assert int(err.item()) == 0
+    del gr  # release the graph's memory pool now, not at some later collection
+    torch.cuda.synchronize()

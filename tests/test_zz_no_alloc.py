@@ -12,6 +12,8 @@ is collected last so that a stop-at-first-failure run has already run every
 other test.
 """
 
+import gc
+
 import pytest
 import torch
 
@@ -84,6 +86,8 @@ def test_static_scratch_matches_oracle_and_allocates_nothing():
             case.page_size, case.scale, out=out, lse=lse, dev_err=err)
 
     call()                      # the first call on a device may load the library's module
+    torch.cuda.synchronize()
+    gc.collect()                # earlier tests' garbage is not freed inside the window below
     torch.cuda.synchronize()
     free0, _ = torch.cuda.mem_get_info()
     used0 = torch.cuda.memory_allocated()
