@@ -159,3 +159,21 @@ def test_item_schedule_sorted_windows_and_round_robin(n_tiles):
     rows = _sampled_rows(c, 400, n_tiles)
     ro, rl = _oracle(c, rows=rows)
     assert_attention_close(out, lse, ro, rl, rows=rows, tag=f"{n_tiles} tiles")
+
+
+def test_item_schedule_one_head_items():
+    """GQA group 1 (one head per item, 16 items per query tile): the sort
+    windows are then 8 * 152 / 16 = 76 tiles; 300 query tiles of documents
+    U[64, 1200] on sampled rows."""
+    T = 300 * 128 - 5
+    rng = np.random.default_rng(300)
+    lens = []
+    while sum(lens) < T:
+        lens.append(int(rng.integers(64, 1201)))
+    lens[-1] = T - sum(lens[:-1])
+    c = W.packed_prefill(10, doc_lens=lens, hq=16, hkv=16)
+    out, lse, err = _run(c)
+    assert err == 0
+    rows = _sampled_rows(c, 400, 300)
+    ro, rl = _oracle(c, rows=rows)
+    assert_attention_close(out, lse, ro, rl, rows=rows, tag="G=1")

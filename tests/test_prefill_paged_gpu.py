@@ -217,3 +217,16 @@ def test_item_schedule_round_robin_above_768_tiles():
     ro, rl, bad_tok, bad = oracle_chunked(c, rows=rows)
     assert not bad_tok and not bad
     assert_attention_close(out, lse, ro, rl, rows=rows, tag="800 tiles")
+
+
+def test_item_schedule_one_head_items():
+    """GQA group 1 (one head per item): 40 chunks of 512 over prefixes
+    U[0, 3000] (160 query tiles) on sampled tokens."""
+    c = W.chunked_prefill(15, n_chunks=40, chunk=512, prefix_lo=0, prefix_hi=3000, n_decode=0,
+                          hq=8, hkv=8)
+    _, _, out, lse, err = run_chunked(c)
+    assert err == 0
+    rows = _sampled_tokens(c, 400, 15)
+    ro, rl, bad_tok, bad = oracle_chunked(c, rows=rows)
+    assert not bad_tok and not bad
+    assert_attention_close(out, lse, ro, rl, rows=rows, tag="G=1 chunks")
