@@ -170,6 +170,14 @@ size_t pkv_decode_workspace_size(const pkv_cache_desc* cache, int batch,
  * address space (unified addressing), so that the results land on the host
  * without a separate copy; the caller synchronises the stream before reading.
  *
+ * q, batch_idx and seq_lens (and k_new, v_new of the fused call) may
+ * likewise be pinned host memory mapped into the device's address space:
+ * the kernels then read them over the host link (q's rows by ordinary
+ * asynchronous copies, the rest by plain loads), so a step needs no input
+ * copy; the host must not rewrite them before the call has completed. q in
+ * pageable host memory, which the GPU cannot read, returns PKV_ERR_ARG. The
+ * pools, the page table, the workspace and dev_err stay in device memory.
+ *
  * workspace: device scratch of at least pkv_decode_workspace_size() bytes,
  * 256-byte aligned, owned by the caller; its contents need no initialisation
  * and are overwritten; calls that share a workspace must be stream-ordered.

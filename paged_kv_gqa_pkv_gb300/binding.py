@@ -144,11 +144,16 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _need(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int):
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int, host_ok: bool = False):
+    """A contiguous tensor of `dtype` and rank `ndim` on the GPU, or (with
+    host_ok) in pinned host memory, which the decode kernels read over the
+    host link."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.dtype != dtype or t.dim() != ndim or not t.is_cuda or not t.is_contiguous():
-        raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor of rank {ndim}, "
+    where_ok = t.is_cuda or (host_ok and t.device.type == "cpu" and t.is_pinned())
+    if t.dtype != dtype or t.dim() != ndim or not where_ok or not t.is_contiguous():
+        kind = "CUDA or pinned host" if host_ok else "CUDA"
+        raise ValueError(f"{name}: expected a contiguous {kind} {dtype} tensor of rank {ndim}, "
                          f"got {t.dtype} {tuple(t.shape)} on {t.device}")
 
 
@@ -230,23 +235,23 @@ def pkv_decode_attention(k_pool, v_pool, page_table, q, batch_idx, seq_lens,
                          workspace=None, dev_err=None, stream=None):
     """Split-KV GQA decode. q [B, Hq, D] bf16 -> (out [B, Hq, D] bf16,
     lse [B, Hq] fp32)."""
-    _need(q, "q", torch.bfloat16, 3)
-    for name, t, dt, nd in (("k_pool", k_pool, torch.bfloat16, 3),
-                            ("v_pool", v_pool, torch.bfloat16, 3),
-                            ("page_table", page_table, torch.int32, 2),
-                            ("batch_idx", batch_idx, torch.int32, 1),
-                            ("seq_lens", seq_lens, torch.int32, 1)):
-        _need(t, name, dt, nd)
+    _need(q, "q", torch.bfloat16, 3, host_ok=True)
+    for name, t, dt, nd, h in (("k_pool", k_pool, torch.bfloat16, 3, False),
+                               ("v_pool", v_pool, torch.bfloat16, 3, False),
+                               ("page_table", page_table, torch.int32, 2, False),
+                               ("batch_idx", batch_idx, torch.int32, 1, True),
+                               ("seq_lens", seq_lens, torch.int32, 1, True)):
+        _need(t, name, dt, nd, host_ok=h)
     B, hq, d = q.shape
     if out is None:
-        out = torch.empty((B, hq, d), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((B, hq, d), dtype=torch.bfloat16, device=k_pool.device)
     if lse is None:
-        lse = torch.empty((B, hq), dtype=torch.float32, device=q.device)
+        lse = torch.empty((B, hq), dtype=torch.float32, device=k_pool.device)
     desc = cache_desc(k_pool, page_table, page_size)
     lib = load_library()
     if workspace is None:
         n = lib.pkv_decode_workspace_size(ctypes.byref(desc), B, hq, 0)
-        workspace = torch.empty(max(int(n), 256), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(max(int(n), 256), dtype=torch.uint8, device=k_pool.device)
     st = lib.pkv_decode_attention(
         ctypes.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(q), hq,
         _ptr(batch_idx), _ptr(seq_lens), B, float(scale), _ptr(out), _ptr(lse),
@@ -262,27 +267,27 @@ def pkv_decode_append_attention(k_pool, v_pool, page_table, q, k_new, v_new, bat
     """One decode step in one call: row b's new token (k_new/v_new
     [B, Hkv, D] bf16) is written to position seq_lens[b] - 1 of its slot and
     attended with the rest. Returns (out [B, Hq, D] bf16, lse [B, Hq] fp32)."""
-    _need(q, "q", torch.bfloat16, 3)
-    for name, t, dt, nd in (("k_pool", k_pool, torch.bfloat16, 3),
-                            ("v_pool", v_pool, torch.bfloat16, 3),
-                            ("k_new", k_new, torch.bfloat16, 3),
-                            ("v_new", v_new, torch.bfloat16, 3),
-                            ("page_table", page_table, torch.int32, 2),
-                            ("batch_idx", batch_idx, torch.int32, 1),
-                            ("seq_lens", seq_lens, torch.int32, 1)):
-        _need(t, name, dt, nd)
+    _need(q, "q", torch.bfloat16, 3, host_ok=True)
+    for name, t, dt, nd, h in (("k_pool", k_pool, torch.bfloat16, 3, False),
+                               ("v_pool", v_pool, torch.bfloat16, 3, False),
+                               ("k_new", k_new, torch.bfloat16, 3, True),
+                               ("v_new", v_new, torch.bfloat16, 3, True),
+                               ("page_table", page_table, torch.int32, 2, False),
+                               ("batch_idx", batch_idx, torch.int32, 1, True),
+                               ("seq_lens", seq_lens, torch.int32, 1, True)):
+        _need(t, name, dt, nd, host_ok=h)
     B, hq, d = q.shape
     if k_new.shape != (B, k_pool.shape[1], d) or v_new.shape != k_new.shape:
         raise ValueError("k_new/v_new must be [B, Hkv, D]")
     if out is None:
-        out = torch.empty((B, hq, d), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((B, hq, d), dtype=torch.bfloat16, device=k_pool.device)
     if lse is None:
-        lse = torch.empty((B, hq), dtype=torch.float32, device=q.device)
+        lse = torch.empty((B, hq), dtype=torch.float32, device=k_pool.device)
     desc = cache_desc(k_pool, page_table, page_size)
     lib = load_library()
     if workspace is None:
         n = lib.pkv_decode_workspace_size(ctypes.byref(desc), B, hq, 0)
-        workspace = torch.empty(max(int(n), 256), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(max(int(n), 256), dtype=torch.uint8, device=k_pool.device)
     st = lib.pkv_decode_append_attention(
         ctypes.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(q), hq,
         _ptr(k_new), _ptr(v_new), _ptr(batch_idx), _ptr(seq_lens), B, float(scale), _ptr(out),
@@ -366,18 +371,18 @@ def pkv_decode_attention_static_scratch(k_pool, v_pool, page_table, q, batch_idx
     """Decode for callers that cannot allocate device memory: same result as
     ``pkv_decode_attention``, with the library's built-in 8 MiB scratch array
     instead of a caller workspace (calls must not overlap on the GPU)."""
-    _need(q, "q", torch.bfloat16, 3)
-    for name, t, dt, nd in (("k_pool", k_pool, torch.bfloat16, 3),
-                            ("v_pool", v_pool, torch.bfloat16, 3),
-                            ("page_table", page_table, torch.int32, 2),
-                            ("batch_idx", batch_idx, torch.int32, 1),
-                            ("seq_lens", seq_lens, torch.int32, 1)):
-        _need(t, name, dt, nd)
+    _need(q, "q", torch.bfloat16, 3, host_ok=True)
+    for name, t, dt, nd, h in (("k_pool", k_pool, torch.bfloat16, 3, False),
+                               ("v_pool", v_pool, torch.bfloat16, 3, False),
+                               ("page_table", page_table, torch.int32, 2, False),
+                               ("batch_idx", batch_idx, torch.int32, 1, True),
+                               ("seq_lens", seq_lens, torch.int32, 1, True)):
+        _need(t, name, dt, nd, host_ok=h)
     B, hq, d = q.shape
     if out is None:
-        out = torch.empty((B, hq, d), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((B, hq, d), dtype=torch.bfloat16, device=k_pool.device)
     if lse is None:
-        lse = torch.empty((B, hq), dtype=torch.float32, device=q.device)
+        lse = torch.empty((B, hq), dtype=torch.float32, device=k_pool.device)
     desc = cache_desc(k_pool, page_table, page_size)
     st = load_library().pkv_decode_attention_static_scratch(
         ctypes.byref(desc), _ptr(k_pool), _ptr(v_pool), _ptr(page_table), _ptr(q), hq,

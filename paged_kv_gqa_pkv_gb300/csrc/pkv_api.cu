@@ -152,6 +152,13 @@ pkv_status decode_entry(const pkv_cache_desc* cache, const void* k_pool, const v
   const size_t need = pkv::decode_workspace_bytes(batch, cache->num_kv_heads, group, workers);
   if (workspace == nullptr || workspace_bytes < need) return PKV_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return PKV_ERR_ALIGN;
+  // q may sit in mapped pinned host memory (its rows then arrive by cp.async,
+  // read over the host link); pageable host memory the GPU cannot reach
+  cudaPointerAttributes qa;
+  const cudaError_t qe = cudaPointerGetAttributes(&qa, q);
+  if (qe != cudaSuccess) return pkv::record_cuda_status(qe);
+  if (qa.type == cudaMemoryTypeUnregistered || qa.devicePointer == nullptr) return PKV_ERR_ARG;
+  const bool q_host = qa.type == cudaMemoryTypeHost;
 
   CUtensorMap kmap, vmap;
   st = encode_pool_map(&kmap, k_pool, cache);
@@ -160,7 +167,8 @@ pkv_status decode_entry(const pkv_cache_desc* cache, const void* k_pool, const v
   if (st != PKV_OK) return st;
 
   pkv::DecodeParams p;
-  p.q = q;
+  p.q = q_host ? qa.devicePointer : q;
+  p.q_host = q_host ? 1 : 0;
   p.page_table = page_table;
   p.batch_idx = batch_idx;
   p.seq_lens = seq_lens;
@@ -434,6 +442,7 @@ pkv_status pkv_mixed_attention(const pkv_cache_desc* cache, const void* k_pool,
   // 3. the listed tokens through the split-KV decode and its merge
   pkv::DecodeParams p;
   p.q = q;
+  p.q_host = 0;
   p.page_table = page_table;
   p.batch_idx = batch_idx;
   p.seq_lens = nullptr;

@@ -384,6 +384,22 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
   const uint8_t* qbase = static_cast<const uint8_t*>(p.q);
   auto issue = [&](const Cursor& c, int k) {
     if (c.b != rp.b) load_row_pages(rp, p, s_slot, c.b, c.tiles, lane);
+    const bool seg_start = (k == 0) || (c.tile == 0);
+    if (seg_start && p.q_host) {
+      // q in mapped host memory: every lane copies its 16-byte pieces of the
+      // item's G rows with cp.async and counts them on the stage barrier
+      // before lane 0 arms it for the K/V bytes, so the stage completes only
+      // once q has landed too
+      const int s = k % S;
+      uint8_t* st = stages + s * C::kStageStride;
+      const int qrow = kList ? s_tok[c.b] : c.b;
+      const uint8_t* src =
+          qbase + (static_cast<size_t>(qrow) * p.num_q_heads + static_cast<size_t>(c.kvh) * G) *
+                      kHeadDim * 2;
+      for (int o = lane * 16; o < C::kQBytes; o += 32 * 16) cp_async16(st + C::kOffQ + o, src + o);
+      cp_async_mbar_arrive(&bars[s]);
+      __syncwarp();
+    }
     if (lane == 0) {
       const int s = k % S;
       uint8_t* st = stages + s * C::kStageStride;
@@ -400,11 +416,11 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
         }
       }
       const int row = page * p.page_size + t0 % p.page_size;
-      const bool seg_start = (k == 0) || (c.tile == 0);
-      mbar_arrive_expect_tx(&bars[s], 2 * kKTileBytes + (seg_start ? C::kQBytes : 0));
+      const bool q_bulk = seg_start && !p.q_host;
+      mbar_arrive_expect_tx(&bars[s], 2 * kKTileBytes + (q_bulk ? C::kQBytes : 0));
       tma_load_4d(st, &kmap, &bars[s], 0, row, 0, c.kvh);
       tma_load_4d(st + C::kOffV, &vmap, &bars[s], 0, row, 0, c.kvh);
-      if (seg_start) {
+      if (q_bulk) {
         const int qrow = kList ? s_tok[c.b] : c.b;
         const size_t qoff =
             (static_cast<size_t>(qrow) * p.num_q_heads + static_cast<size_t>(c.kvh) * G) *

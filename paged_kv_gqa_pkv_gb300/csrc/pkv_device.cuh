@@ -112,6 +112,21 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared through L2: an ordinary async
+// copy, not a bulk one, so its source may be mapped (pinned) host memory.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+
+// The calling thread's earlier cp.async copies arrive on `bar` once they have
+// completed. The barrier's pending count rises now (no .noinc), so a phase
+// armed after this call cannot complete before those copies land.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
 // ------------------------------------------- programmatic dependent launch --
 
 // Blocks until the grid this launch depends on has completed and its memory

@@ -68,6 +68,7 @@ struct DecodeParams {
   const int32_t* row_count;
   const int32_t* input_pos;
   int32_t* dev_err;
+  int q_host;                 // q is mapped host memory: its rows arrive by cp.async
   int batch;
   int num_q_heads;
   int num_kv_heads;

@@ -3,6 +3,8 @@ decode workloads at full size and on edge cases (tile edges, empty rows,
 padding rows, NaN garbage in unused slots, bad entries, other GQA groups,
 changing batch sizes in one process)."""
 
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -278,3 +280,113 @@ def test_workspace_needs_no_initialisation(fill):
     assert int(err.item()) == 0
     del gr  # release the graph's memory pool now, not at some later collection
     torch.cuda.synchronize()
+
+
+def _pinned(t):
+    return t.contiguous().pin_memory()
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (32, 8), (32, 4)])
+def test_host_resident_inputs_give_the_same_bits(hq, hkv):
+    """q, batch_idx and seq_lens in pinned host memory (the kernels read them
+    over the host link; q's rows by cp.async) give the bits the same call
+    gives on device copies, for GQA groups 1, 4 and 8."""
+    lens = torch.randint(1, 3000, (33,), generator=torch.Generator().manual_seed(hq + hkv)).tolist()
+    lens[3] = 0
+    c = W.custom_decode(60 + hq, lens, hq=hq, hkv=hkv, page_size=128, permute=True, n_pad=3)
+    kp, vp, table = gpu(c.k_pool), gpu(c.v_pool), gpu(c.page_table)
+    err = new_dev_err()
+    o_dev, l_dev = binding.pkv_decode_attention(kp, vp, table, gpu(c.q), gpu(c.batch_idx),
+                                                gpu(c.seq_lens), c.page_size, c.scale,
+                                                dev_err=err)
+    o_host, l_host = binding.pkv_decode_attention(kp, vp, table, _pinned(c.q),
+                                                  _pinned(c.batch_idx), _pinned(c.seq_lens),
+                                                  c.page_size, c.scale, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(o_host, o_dev) and torch.equal(l_host, l_dev)
+    _, _, ref_o, ref_l, _, _ = oracle_decode_step(c, append=False)
+    assert_attention_close(o_host.cpu(), l_host.cpu(), ref_o, ref_l, tag="host inputs")
+
+
+def test_host_resident_inputs_fused_step_and_graph_replay():
+    """The fused append + decode with q, k_new, v_new, batch_idx and
+    seq_lens in pinned host memory and out/lse written to pinned host memory:
+    the pools and results equal those of the same step on device inputs, and
+    a captured step replayed after the host rewrote its inputs in place gives
+    the new step's bits."""
+    c = W.qwen3_b64_decode(4, permute=True)
+    c2 = W.qwen3_b64_decode(5, permute=True)  # other q / k_new / v_new, same lengths
+    kp_d, vp_d = gpu(c.k_pool), gpu(c.v_pool)
+    kp_h, vp_h = gpu(c.k_pool), gpu(c.v_pool)
+    table = gpu(c.page_table)
+    err = new_dev_err()
+    o_d, l_d = binding.pkv_decode_append_attention(
+        kp_d, vp_d, table, gpu(c.q), gpu(c.k_new), gpu(c.v_new), gpu(c.batch_idx),
+        gpu(c.seq_lens), c.page_size, c.scale, dev_err=err)
+    hq_, hk, hv = _pinned(c.q), _pinned(c.k_new), _pinned(c.v_new)
+    hb, hs = _pinned(c.batch_idx), _pinned(c.seq_lens)
+    out_h = torch.empty((c.batch, c.num_q_heads, 128), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((c.batch, c.num_q_heads), dtype=torch.float32).pin_memory()
+    binding.pkv_decode_append_attention(kp_h, vp_h, table, hq_, hk, hv, hb, hs, c.page_size,
+                                        c.scale, out=out_h, lse=lse_h, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(kp_h, kp_d) and torch.equal(vp_h, vp_d)
+    assert torch.equal(out_h, o_d.cpu()) and torch.equal(lse_h, l_d.cpu())
+    # capture the host-input step, then rewrite the inputs in place and replay
+    ws = torch.empty(binding.pkv_decode_workspace_size(kp_h, table, c.page_size, c.batch,
+                                                       c.num_q_heads),
+                     dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+
+    def step():
+        binding.pkv_decode_append_attention(kp_h, vp_h, table, hq_, hk, hv, hb, hs,
+                                            c.page_size, c.scale, out=out_h, lse=lse_h,
+                                            workspace=ws, dev_err=err)
+
+    with torch.cuda.stream(s):
+        step()
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            step()
+    torch.cuda.synchronize()
+    hq_.copy_(c2.q)
+    hk.copy_(c2.k_new)
+    hv.copy_(c2.v_new)
+    kp2, vp2 = gpu(c.k_pool), gpu(c.v_pool)
+    o2, l2 = binding.pkv_decode_append_attention(
+        kp2, vp2, table, gpu(c2.q), gpu(c2.k_new), gpu(c2.v_new), gpu(c.batch_idx),
+        gpu(c.seq_lens), c.page_size, c.scale, dev_err=err)
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(kp_h, kp2) and torch.equal(vp_h, vp2)
+    assert torch.equal(out_h, o2.cpu()) and torch.equal(lse_h, l2.cpu())
+    del g
+
+
+def test_pageable_host_q_is_rejected():
+    """q in pageable host memory, which the GPU cannot read, is refused at the
+    C boundary (PKV_ERR_ARG) before any launch."""
+    c = W.tiny_decode(0)
+    kp, vp, table = gpu(c.k_pool), gpu(c.v_pool), gpu(c.page_table)
+    q_pageable = c.q.clone()  # not pinned
+    lib = binding.load_library()
+    desc = binding.cache_desc(kp, table, c.page_size)
+    need = lib.pkv_decode_workspace_size(ctypes.byref(desc), c.batch, c.num_q_heads, 0)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    out = torch.empty((c.batch, c.num_q_heads, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((c.batch, c.num_q_heads), dtype=torch.float32, device="cuda")
+    bi, sl = gpu(c.batch_idx), gpu(c.seq_lens)
+    st = lib.pkv_decode_attention(
+        ctypes.byref(desc), ctypes.c_void_p(kp.data_ptr()), ctypes.c_void_p(vp.data_ptr()),
+        ctypes.c_void_p(table.data_ptr()), ctypes.c_void_p(q_pageable.data_ptr()),
+        c.num_q_heads, ctypes.c_void_p(bi.data_ptr()), ctypes.c_void_p(sl.data_ptr()), c.batch,
+        ctypes.c_float(c.scale), ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr()),
+        ctypes.c_void_p(ws.data_ptr()), ctypes.c_size_t(need), None,
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 1  # PKV_ERR_ARG
+    with pytest.raises(ValueError):
+        binding.pkv_decode_attention(kp, vp, table, q_pageable, bi, sl, c.page_size, c.scale)
