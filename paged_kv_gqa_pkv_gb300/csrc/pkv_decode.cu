@@ -158,16 +158,22 @@ __device__ __forceinline__ void advance(Cursor& c, const int32_t* prefix, int hk
 
 // Fused append: the new token of item (b, kvh), at position seq_lens[b] - 1,
 // copied from k_new/v_new into the pools (lanes 0-15 a K chunk of 16 bytes,
-// lanes 16-31 a V chunk). Only the warp that reads the item's last tile
-// calls this, before its own TMA read of that tile.
-__device__ __forceinline__ void append_new_token(const DecodeParams& p, const int32_t* s_slot,
-                                                 const int32_t* s_len, int b, int kvh, int lane) {
+// lanes 16-31 a V chunk). Only the warp that reads the item's last tile does
+// this, before its own TMA read of that tile.
+// Split in two so that a warp can issue the loads of several items before
+// their stores (k_new/v_new may be host memory, a link round trip away).
+__device__ __forceinline__ uint4 append_load(const DecodeParams& p, int b, int kvh, int lane) {
+  const int64_t src = (static_cast<int64_t>(b) * p.num_kv_heads + kvh) * kHeadDim + (lane & 15) * 8;
+  return *reinterpret_cast<const uint4*>(
+      static_cast<const __nv_bfloat16*>(lane < 16 ? p.k_new : p.v_new) + src);
+}
+
+__device__ __forceinline__ void append_store(const DecodeParams& p, const int32_t* s_slot,
+                                             const int32_t* s_len, int b, int kvh, int lane,
+                                             const uint4 val) {
   const int n = s_len[b];
   const int pos = n - 1;
   const int hkv = p.num_kv_heads;
-  const int64_t src = (static_cast<int64_t>(b) * hkv + kvh) * kHeadDim + (lane & 15) * 8;
-  const uint4 val = *reinterpret_cast<const uint4*>(
-      static_cast<const __nv_bfloat16*>(lane < 16 ? p.k_new : p.v_new) + src);
   const int page = p.page_table[static_cast<int64_t>(s_slot[b]) * p.max_blocks + pos / p.page_size];
   if (page < 0 || page >= p.num_pages) {
     if (lane == 0) set_dev_err(p.dev_err, PKV_DEV_ERR_BAD_PAGE);
@@ -435,16 +441,37 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
   if (p.k_new != nullptr) {
     // Fused append: this warp owns the new tokens of the items whose last
     // tile lies in its range. They reach the pools before any TMA read here.
+    // Four items at a time: their loads all go out before the first store.
     Cursor c = start;
     int64_t u = u_begin;
-    while (true) {
-      const int64_t u_last = u + (c.tiles - 1 - c.tile);
-      if (u_last >= u_end) break;
-      append_new_token(p, s_slot, s_len, c.b, c.kvh, lane);
-      u = u_last + 1;
-      if (u >= u_end) break;
-      c.tile = c.tiles - 1;
-      advance(c, s_prefix, hkv);
+    bool more = true;
+    while (more) {
+      int nb = 0;
+      int ib[4], ik[4];
+      while (nb < 4) {
+        const int64_t u_last = u + (c.tiles - 1 - c.tile);
+        if (u_last >= u_end) {
+          more = false;
+          break;
+        }
+        ib[nb] = c.b;
+        ik[nb] = c.kvh;
+        ++nb;
+        u = u_last + 1;
+        if (u >= u_end) {
+          more = false;
+          break;
+        }
+        c.tile = c.tiles - 1;
+        advance(c, s_prefix, hkv);
+      }
+      uint4 val[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (e < nb) val[e] = append_load(p, ib[e], ik[e], lane);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (e < nb) append_store(p, s_slot, s_len, ib[e], ik[e], lane, val[e]);
     }
     fence_proxy_async_global();
     __syncwarp();
