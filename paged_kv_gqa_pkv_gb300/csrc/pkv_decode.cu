@@ -438,49 +438,75 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
 
   load_row_pages(rp, p, s_slot, start.b, start.tiles, lane);
   pdl_wait_primary();
-  if (p.k_new != nullptr) {
-    // Fused append: this warp owns the new tokens of the items whose last
-    // tile lies in its range. They reach the pools before any TMA read here.
-    // Four items at a time: their loads all go out before the first store.
-    Cursor c = start;
-    int64_t u = u_begin;
-    bool more = true;
-    while (more) {
-      int nb = 0;
-      int ib[4], ik[4];
-      while (nb < 4) {
-        const int64_t u_last = u + (c.tiles - 1 - c.tile);
-        if (u_last >= u_end) {
-          more = false;
-          break;
-        }
-        ib[nb] = c.b;
-        ik[nb] = c.kvh;
-        ++nb;
-        u = u_last + 1;
-        if (u >= u_end) {
-          more = false;
-          break;
-        }
-        c.tile = c.tiles - 1;
-        advance(c, s_prefix, hkv);
+  // Fused append: this warp owns the new tokens of the items whose last tile
+  // lies in its range, and they must reach the pools before its TMA read of
+  // that tile. The loads of the first four go out now; their stores follow
+  // once the first stages are issued, or before a stage that reads one of
+  // those tiles, so streaming does not start a round trip (to the host, when
+  // k_new/v_new live there) late. Items past the first four (their last
+  // tiles lie past the first stages) are appended four at a time after that.
+  Cursor ac = start;
+  int64_t au = u_begin;
+  bool amore = p.k_new != nullptr;
+  int nb = 0;
+  int ib[4], ik[4];
+  int64_t ul[4];  // tile-list index of each pending item's last tile
+  uint4 val[4];
+  // the next up to four owned items from (ac, au)
+  auto gather = [&]() {
+    nb = 0;
+    while (amore && nb < 4) {
+      const int64_t u_last = au + (ac.tiles - 1 - ac.tile);
+      if (u_last >= u_end) {
+        amore = false;
+        break;
       }
-      uint4 val[4];
+      ib[nb] = ac.b;
+      ik[nb] = ac.kvh;
+      ul[nb] = u_last;
+      ++nb;
+      au = u_last + 1;
+      if (au >= u_end) {
+        amore = false;
+        break;
+      }
+      ac.tile = ac.tiles - 1;
+      advance(ac, s_prefix, hkv);
+    }
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (e < nb) val[e] = append_load(p, ib[e], ik[e], lane);
+    for (int e = 0; e < 4; ++e)
+      if (e < nb) val[e] = append_load(p, ib[e], ik[e], lane);
+  };
+  auto store_pending = [&]() {
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (e < nb) append_store(p, s_slot, s_len, ib[e], ik[e], lane, val[e]);
+    for (int e = 0; e < 4; ++e)
+      if (e < nb) append_store(p, s_slot, s_len, ib[e], ik[e], lane, val[e]);
+    nb = 0;
+  };
+  bool appended = p.k_new == nullptr;
+  auto finish_append = [&]() {
+    if (appended) return;
+    store_pending();
+    while (amore) {
+      gather();
+      store_pending();
     }
     fence_proxy_async_global();
     __syncwarp();
-  }
+    appended = true;
+  };
+  if (!appended) gather();
   const int prologue = min(S, count);
   for (int k = 0; k < prologue; ++k) {
+    bool reads_pending = false;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (e < nb && ul[e] == u_begin + k) reads_pending = true;
+    if (reads_pending) finish_append();
     issue(pc, k);
     if (k + 1 < count) advance(pc, s_prefix, hkv);
   }
+  finish_append();
 
   // MMA fragment coordinates: g = this lane's accumulator row (a token in
   // S^T, a head dim in O^T), t = its column pair (query heads 2t, 2t+1).
