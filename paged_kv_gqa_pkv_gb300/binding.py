@@ -4,6 +4,9 @@ Argument marshalling only: shapes are read from the tensors, outputs are
 allocated with PyTorch when the caller passes none, and every computation
 runs in the library's CUDA kernels on the caller's current stream. There is
 no fallback: if ``libpkv.so`` is missing or fails to load, every call raises.
+Tensors live on the GPU, except that the decode calls also take q,
+batch_idx, seq_lens, k_new, v_new, out and lse as pinned host tensors, which
+the kernels read or write over the host link (no copy).
 
 Functions keep the names of the C entry points: ``pkv_append``,
 ``pkv_append_rope``, ``pkv_decode_workspace_size``, ``pkv_decode_attention``,
@@ -234,7 +237,9 @@ def pkv_decode_attention(k_pool, v_pool, page_table, q, batch_idx, seq_lens,
                          page_size: int, scale: float, out=None, lse=None,
                          workspace=None, dev_err=None, stream=None):
     """Split-KV GQA decode. q [B, Hq, D] bf16 -> (out [B, Hq, D] bf16,
-    lse [B, Hq] fp32)."""
+    lse [B, Hq] fp32). q, batch_idx and seq_lens may be pinned host tensors,
+    and out/lse pinned host tensors too; the outputs default to the pools'
+    device."""
     _need(q, "q", torch.bfloat16, 3, host_ok=True)
     for name, t, dt, nd, h in (("k_pool", k_pool, torch.bfloat16, 3, False),
                                ("v_pool", v_pool, torch.bfloat16, 3, False),
