@@ -139,7 +139,9 @@ pkv_status pkv_append_rope(const pkv_cache_desc* cache, void* k_pool, void* v_po
  * on the CURRENT device for `batch` rows and `num_q_heads` query heads.
  * max_seq_len is accepted for interface stability; the split-KV schedule
  * balances work over the device's SMs and its scratch does not grow with
- * sequence length. Returns 0 for invalid arguments.
+ * sequence length. A batch above 512 rows runs as equal launches of at most
+ * 512 rows that reuse the workspace, so the size is that of one launch.
+ * Returns 0 for invalid arguments.
  */
 size_t pkv_decode_workspace_size(const pkv_cache_desc* cache, int batch,
                                  int num_q_heads, int max_seq_len);
@@ -151,7 +153,9 @@ size_t pkv_decode_workspace_size(const pkv_cache_desc* cache, int batch,
  * (enable_gqa); zero-safe padded rows: "flex_vs_vllm.md", "What broke
  * correctness and had to be dropped" (ROWS_GUARANTEED_SAFE).
  *
- * batch may be 0..512 per call (larger batches: split them over calls).
+ * batch may be any count >= 0. Above 512 rows (the kernels' row tables in
+ * shared memory) the call enqueues equal launches of at most 512 rows each,
+ * in row order on `stream`, sharing the workspace.
  * Row b in [0, batch) has one query token q[b] (bf16 [num_q_heads, D] within
  * a contiguous [batch, num_q_heads, D] tensor) and attends the first
  * n = seq_lens[b] logical keys of slot c = batch_idx[b] (for a decode step

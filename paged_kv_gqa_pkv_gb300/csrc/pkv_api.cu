@@ -134,7 +134,7 @@ pkv_status decode_entry(const pkv_cache_desc* cache, const void* k_pool, const v
                         cudaStream_t stream) {
   pkv_status st = check_cache(cache);
   if (st != PKV_OK) return st;
-  if (batch < 0 || batch > pkv::kDecodeMaxBatch) return PKV_ERR_ARG;
+  if (batch < 0) return PKV_ERR_ARG;
   if (!group_ok(num_q_heads, cache->num_kv_heads)) return PKV_ERR_ARG;
   if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return PKV_ERR_ARG;
   if (batch == 0) return PKV_OK;
@@ -149,7 +149,13 @@ pkv_status decode_entry(const pkv_cache_desc* cache, const void* k_pool, const v
   if (st != PKV_OK) return st;
   const int group = num_q_heads / cache->num_kv_heads;
   const int workers = pkv::decode_workers_for_device(sms);
-  const size_t need = pkv::decode_workspace_bytes(batch, cache->num_kv_heads, group, workers);
+  // A batch past the kernels' row tables runs as consecutive launches of at
+  // most kDecodeMaxBatch rows each, equal in size, on the caller's stream;
+  // they reuse one workspace in stream order.
+  const int launches = (batch + pkv::kDecodeMaxBatch - 1) / pkv::kDecodeMaxBatch;
+  const int rows_per_launch = (batch + launches - 1) / launches;
+  const size_t need =
+      pkv::decode_workspace_bytes(rows_per_launch, cache->num_kv_heads, group, workers);
   if (workspace == nullptr || workspace_bytes < need) return PKV_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return PKV_ERR_ALIGN;
   // q may sit in mapped pinned host memory (its rows then arrive by cp.async,
@@ -192,7 +198,25 @@ pkv_status decode_entry(const pkv_cache_desc* cache, const void* k_pool, const v
   p.max_blocks = cache->max_blocks;
   p.num_workers = workers;
   p.qscale = scale * 1.4426950408889634f;
-  return cuda_status(pkv::launch_decode(p, kmap, vmap, sms, stream));
+  if (launches == 1) return cuda_status(pkv::launch_decode(p, kmap, vmap, sms, stream));
+  const size_t q_row = static_cast<size_t>(num_q_heads) * cache->head_dim * 2;
+  const size_t kv_row = static_cast<size_t>(cache->num_kv_heads) * cache->head_dim * 2;
+  for (int r0 = 0; r0 < batch; r0 += rows_per_launch) {
+    pkv::DecodeParams pr = p;
+    pr.batch = batch - r0 < rows_per_launch ? batch - r0 : rows_per_launch;
+    pr.q = static_cast<const uint8_t*>(p.q) + r0 * q_row;
+    pr.batch_idx = batch_idx + r0;
+    pr.seq_lens = seq_lens + r0;
+    pr.out = static_cast<uint8_t*>(out) + r0 * q_row;
+    pr.lse = lse + static_cast<size_t>(r0) * num_q_heads;
+    if (k_new != nullptr) {
+      pr.k_new = static_cast<const uint8_t*>(k_new) + r0 * kv_row;
+      pr.v_new = static_cast<const uint8_t*>(v_new) + r0 * kv_row;
+    }
+    const pkv_status s = cuda_status(pkv::launch_decode(pr, kmap, vmap, sms, stream));
+    if (s != PKV_OK) return s;
+  }
+  return PKV_OK;
 }
 
 // Workspace of pkv_mixed_attention: the routed-token and query-tile counts,
@@ -331,11 +355,15 @@ pkv_status pkv_append_rope(const pkv_cache_desc* cache, void* k_pool, void* v_po
 size_t pkv_decode_workspace_size(const pkv_cache_desc* cache, int batch, int num_q_heads,
                                  int max_seq_len) {
   (void)max_seq_len;
-  if (check_cache(cache) != PKV_OK || batch < 0 || batch > pkv::kDecodeMaxBatch) return 0;
+  if (check_cache(cache) != PKV_OK || batch < 0) return 0;
   if (!group_ok(num_q_heads, cache->num_kv_heads)) return 0;
   int sms = 0;
   if (device_info(&sms) != PKV_OK) return 0;
-  return pkv::decode_workspace_bytes(batch, cache->num_kv_heads,
+  // rows of one launch: larger batches run as equal launches of at most
+  // kDecodeMaxBatch rows that reuse the workspace
+  const int launches = (batch + pkv::kDecodeMaxBatch - 1) / pkv::kDecodeMaxBatch;
+  const int rows = launches > 1 ? (batch + launches - 1) / launches : batch;
+  return pkv::decode_workspace_bytes(rows, cache->num_kv_heads,
                                      num_q_heads / cache->num_kv_heads,
                                      pkv::decode_workers_for_device(sms));
 }

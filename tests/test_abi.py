@@ -95,7 +95,10 @@ def test_decode_rejects_bad_arguments(lib):
     assert lib.pkv_decode_attention(*args(hq=6)) == 1          # group 3
     assert lib.pkv_decode_attention(*args(hq=32)) == 1         # group 16
     assert lib.pkv_decode_attention(*args(batch=-1)) == 1
-    assert lib.pkv_decode_attention(*args(batch=100000)) == 1  # past the per-call limit
+    # any batch size is accepted (above 512 rows the call runs as several
+    # launches): 100 000 rows pass the argument checks and stop at the
+    # device check without a supported GPU, else at the 1 MiB workspace
+    assert lib.pkv_decode_attention(*args(batch=100000)) in (4, 5)
     assert lib.pkv_decode_attention(*args(q=264)) == 2
     assert lib.pkv_decode_attention(*args(scale=float("nan"))) == 1
     assert lib.pkv_decode_attention(*args(batch=0)) == 0

@@ -134,3 +134,21 @@ def test_results_written_straight_into_pinned_host_memory():
     torch.cuda.synchronize()
     assert e1 == 0 and int(err.item()) == 0
     assert torch.equal(out_h, o1) and torch.equal(lse_h, l1)
+
+
+def test_fused_batches_above_512_rows():
+    """777 rows run as two launches of at most 389 rows: each appends and
+    attends its own rows. Pools and outputs equal the two-call step's bits
+    and the oracle's."""
+    lens = torch.randint(1, 150, (777,), generator=torch.Generator().manual_seed(12)).tolist()
+    c = W.custom_decode(12, lens, hq=32, hkv=8, page_size=16, permute=True)
+    _live_rows_decode_convention(c)
+    k1, v1, o1, l1, e1 = run_fused(c)
+    k2, v2, o2, l2, e2 = run_decode_step(c)
+    assert e1 == 0 and e2 == 0
+    assert torch.equal(k1, k2) and torch.equal(v1, v2)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    ek, ev, ref_o, ref_l, bad_tok, bad_rows = oracle_decode_step(c)
+    assert not bad_tok and not bad_rows
+    assert np.array_equal(bf16_bits(k1), ek) and np.array_equal(bf16_bits(v1), ev)
+    assert_attention_close(o1, l1, ref_o, ref_l, tag="fused 777 rows")

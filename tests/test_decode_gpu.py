@@ -390,3 +390,29 @@ def test_pageable_host_q_is_rejected():
     assert st == 1  # PKV_ERR_ARG
     with pytest.raises(ValueError):
         binding.pkv_decode_attention(kp, vp, table, q_pageable, bi, sl, c.page_size, c.scale)
+
+
+def test_batches_above_512_rows_run_as_equal_launches():
+    """1100 rows (five of them padding) run as three launches of at most 367
+    rows over one workspace, whose size is that of one launch: every row
+    against the oracle, and the same bits with q, batch_idx and seq_lens in
+    pinned host memory (each launch reads its rows at an offset there)."""
+    lens = torch.randint(1, 200, (1095,), generator=torch.Generator().manual_seed(11)).tolist()
+    c = W.custom_decode(11, lens, hq=32, hkv=8, page_size=16, permute=True, n_pad=5)
+    assert c.batch == 1100
+    kp, vp, table = gpu(c.k_pool), gpu(c.v_pool), gpu(c.page_table)
+    size = lambda b: binding.pkv_decode_workspace_size(kp, table, c.page_size, b, c.num_q_heads)
+    assert size(1100) == size(367) < size(512)
+    assert size(1536) == size(512)
+    _, _, o_dev, l_dev, err = run_decode_step(c, append=False)
+    assert err == 0
+    _, _, ref_o, ref_l, _, bad_rows = oracle_decode_step(c, append=False)
+    assert not bad_rows
+    assert_attention_close(o_dev, l_dev, ref_o, ref_l, tag="1100 rows")
+    e2 = new_dev_err()
+    o_host, l_host = binding.pkv_decode_attention(kp, vp, table, _pinned(c.q),
+                                                  _pinned(c.batch_idx), _pinned(c.seq_lens),
+                                                  c.page_size, c.scale, dev_err=e2)
+    torch.cuda.synchronize()
+    assert int(e2.item()) == 0
+    assert torch.equal(o_host.cpu(), o_dev) and torch.equal(l_host.cpu(), l_dev)
