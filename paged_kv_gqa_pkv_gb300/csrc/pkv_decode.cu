@@ -53,6 +53,27 @@ namespace {
 
 constexpr int kKTileBytes = kDecodeTile * kHeadDim * 2;  // one head, 16 tokens (4 KB)
 
+// The K/V stream of a call is read once: its TMA loads carry an L2
+// evict-first policy, so the lines they bring in are the first replaced and
+// the partials, q rows and page-table rows the call reuses stay in L2
+// (decode call 37.70 -> 37.10 us on the B = 64 Qwen3-4B step).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void tma_load_4d_evict_first(void* dst, const CUtensorMap* map,
+                                                        uint64_t* bar, int x, int y, int z, int w,
+                                                        uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w),
+      "l"(pol)
+      : "memory");
+}
+
 template <int G>
 struct DecodeCfg {
   static constexpr int kStages = kDecodeStages;
@@ -388,6 +409,7 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
   bool bail = false;
 
   const uint8_t* qbase = static_cast<const uint8_t*>(p.q);
+  const uint64_t kv_policy = l2_evict_first_policy();
   auto issue = [&](const Cursor& c, int k) {
     if (c.b != rp.b) load_row_pages(rp, p, s_slot, c.b, c.tiles, lane);
     const bool seg_start = (k == 0) || (c.tile == 0);
@@ -424,8 +446,8 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
       const int row = page * p.page_size + t0 % p.page_size;
       const bool q_bulk = seg_start && !p.q_host;
       mbar_arrive_expect_tx(&bars[s], 2 * kKTileBytes + (q_bulk ? C::kQBytes : 0));
-      tma_load_4d(st, &kmap, &bars[s], 0, row, 0, c.kvh);
-      tma_load_4d(st + C::kOffV, &vmap, &bars[s], 0, row, 0, c.kvh);
+      tma_load_4d_evict_first(st, &kmap, &bars[s], 0, row, 0, c.kvh, kv_policy);
+      tma_load_4d_evict_first(st + C::kOffV, &vmap, &bars[s], 0, row, 0, c.kvh, kv_policy);
       if (q_bulk) {
         const int qrow = kList ? s_tok[c.b] : c.b;
         const size_t qoff =
