@@ -789,40 +789,64 @@ decode_splitkv_kernel(const __grid_constant__ CUtensorMap kmap,
   }
 }
 
-// One warp per (row, q head). The warp rebuilds the split-KV schedule from
-// the call's inputs (row tile counts and their prefix) before waiting on the
-// split-KV grid, so after the wait only the partials are read: for items of
-// up to kFast segments (16 with kByCta, else 8), (m, l) and all o rows go out
-// in one round of loads.
-template <int G, bool kByCta, bool kList>
+// One warp per (row, q head). Before waiting on the split-KV grid, the CTA
+// rebuilds that grid's schedule from the call's inputs (each row's tile count
+// and their prefix, one pass over the rows shared by the CTA's 256 threads),
+// so after the wait only the partials are read: for items of up to kFast
+// segments, (m, l) and all o rows go out in one round of loads. kFast is 8,
+// 16 when long items were combined per CTA (kByCta), and 32 (kWide) for
+// launches with few items for the workers, whose items have many segments;
+// kWide keeps 32 o rows in registers, so it is a separate instantiation.
+template <int G, bool kByCta, bool kList, bool kWide>
 __global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p) {
-  constexpr int kFast = kByCta ? 16 : 8;
+  constexpr int kFast = kWide ? 32 : (kByCta ? 16 : 8);
+  __shared__ int32_t s_prefix[kDecodeMaxBatch + 1];
+  __shared__ int32_t s_warp_sum[8];
   // The next launch may start its prologue now; it touches the workspace
   // only after this grid completes.
   pdl_launch_dependents();
-  const int lane = threadIdx.x & 31;
-  const int wid = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int B = call_rows<kList>(p);
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int wid = blockIdx.x * 8 + (tid >> 5);
+  const int B = call_rows<kList>(p);  // at most kDecodeMaxBatch per launch
+  {
+    const int per_thread = (B + 255) / 256;
+    const int r0 = min(tid * per_thread, B);
+    const int r1 = min(r0 + per_thread, B);
+    int local = 0;
+    for (int r = r0; r < r1; ++r) {
+      int err;
+      const int t = row_tiles<kList>(p, r, &err);
+      s_prefix[r] = t;
+      local += t;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_warp_sum[tid >> 5] = incl;
+    __syncthreads();
+    int run = incl - local;
+    for (int w = 0; w < (tid >> 5); ++w) run += s_warp_sum[w];
+    for (int r = r0; r < r1; ++r) {
+      const int t = s_prefix[r];
+      s_prefix[r] = run;
+      run += t;
+    }
+    if (tid == 255) s_prefix[B] = run;
+    __syncthreads();
+  }
   const bool active = wid < B * p.num_q_heads;
   const int b = active ? wid / p.num_q_heads : 0;
   const int h = wid % p.num_q_heads;
   const int kvh = h / G;
   const int g = h % G;
   const int hkv = p.num_kv_heads;
-  int before = 0, total = 0, tiles = 0;
-  for (int r = lane; r < B; r += 32) {
-    int err;
-    const int t = row_tiles<kList>(p, r, &err);
-    total += t;
-    if (r < b) before += t;
-    if (r == b) tiles = t;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    total += __shfl_xor_sync(0xffffffffu, total, o);
-    before += __shfl_xor_sync(0xffffffffu, before, o);
-    tiles += __shfl_xor_sync(0xffffffffu, tiles, o);
-  }
+  const int before = active ? s_prefix[b] : 0;
+  const int tiles = active ? s_prefix[b + 1] - before : 0;
+  const int total = s_prefix[B];
   pdl_wait_primary();
   if (!active) return;
   // output row of (b, h): wid itself, or in list mode that of b's token
@@ -953,9 +977,16 @@ static cudaError_t launch_decode_gc(const DecodeParams& p, const CUtensorMap& km
   e = launch_kernel(decode_splitkv_kernel<G, kCombine, kList>, dim3(sm_count),
                     dim3(kDecodeWarps * 32), smem, stream, /*programmatic=*/true, kmap, vmap, p);
   if (e != cudaSuccess) return e;
+  // Items with many segments (more than ~6 workers per item) take the merge
+  // that loads up to 32 segments in one round.
   const int rows = p.batch * p.num_q_heads;
-  return launch_kernel(decode_merge_kernel<G, kCombine, kList>, dim3((rows + 7) / 8), dim3(256),
-                       0, stream, /*programmatic=*/true, p);
+  const bool wide = !kCombine && static_cast<int64_t>(p.num_workers) >
+                                     static_cast<int64_t>(6) * p.batch * p.num_kv_heads;
+  if (wide)
+    return launch_kernel(decode_merge_kernel<G, kCombine, kList, true>, dim3((rows + 7) / 8),
+                         dim3(256), 0, stream, /*programmatic=*/true, p);
+  return launch_kernel(decode_merge_kernel<G, kCombine, kList, false>, dim3((rows + 7) / 8),
+                       dim3(256), 0, stream, /*programmatic=*/true, p);
 }
 
 // Few (row, kv head) items for the machine's workers means long items: then
