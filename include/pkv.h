@@ -238,8 +238,11 @@ pkv_status pkv_decode_append_attention(const pkv_cache_desc* cache, void* k_pool
  * every GPU that loads the library until the process exits. It allocates
  * nothing and calls no allocating routine.
  *  - A call whose pkv_decode_workspace_size() exceeds 8 MiB returns
- *    PKV_ERR_WORKSPACE without launching (about 350 rows at 8 KV heads and a
- *    GQA group of 4 on a 152-SM GB300; use pkv_decode_attention beyond that).
+ *    PKV_ERR_WORKSPACE without launching (one launch of more than about 350
+ *    rows at 8 KV heads and a GQA group of 4 on a 152-SM GB300; a batch above
+ *    512 rows runs as equal launches, so whether it fits depends on their
+ *    size, which pkv_decode_workspace_size() reflects; use
+ *    pkv_decode_attention where it does not fit).
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current and caches it; make that
  *    first call before any stream capture. A failed lookup returns
