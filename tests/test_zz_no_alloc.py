@@ -69,6 +69,36 @@ def test_static_scratch_rejects_batches_past_its_limit():
     assert e.value.status == 4
 
 
+def test_static_scratch_batches_above_512_rows_run_when_each_launch_fits():
+    """Above 512 rows a call runs as equal launches, and the built-in scratch
+    holds one launch's partials: 1030 rows (three launches of 344 on a 152-SM
+    GB300) fit and give the workspace entry point's bits; 1100 rows (three of
+    367) do not fit and are refused before any launch."""
+    lens = torch.randint(1, 120, (1100,), generator=torch.Generator().manual_seed(21)).tolist()
+    case = W.custom_decode(21, lens, hq=32, hkv=8, page_size=16, permute=True)
+    x = _inputs(case)
+    seen = set()
+    for B in (1030, 1100):
+        args = (x["k_pool"], x["v_pool"], x["page_table"], x["q"][:B].contiguous(),
+                x["batch_idx"][:B].contiguous(), x["seq_lens"][:B].contiguous(),
+                case.page_size, case.scale)
+        need = binding.pkv_decode_workspace_size(x["k_pool"], x["page_table"], case.page_size,
+                                                 B, case.num_q_heads)
+        if need <= 8 << 20:
+            ref_out, ref_lse = binding.pkv_decode_attention(*args)
+            out, lse = binding.pkv_decode_attention_static_scratch(*args)
+            torch.cuda.synchronize()
+            assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
+            seen.add("fits")
+        else:
+            with pytest.raises(binding.PkvError) as e:
+                binding.pkv_decode_attention_static_scratch(*args)
+            assert e.value.status == 4
+            seen.add("refused")
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert seen == {"fits", "refused"}
+
+
 def test_static_scratch_matches_oracle_and_allocates_nothing():
     case = W.tiny_decode(0)
     x = _inputs(case)
