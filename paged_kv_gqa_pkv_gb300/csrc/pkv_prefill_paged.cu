@@ -53,6 +53,26 @@ namespace {
 
 using namespace prefill_detail;
 
+// Each query tile is loaded once per item, while a chunk's K/V tiles are read
+// by all its query tiles: Q's TMA loads carry an L2 evict-first policy, so
+// its lines are the first replaced and the K/V tiles stay in L2 (16 chunks of
+// 512 over prefixes U[512, 4096]: 380 -> 376 us, same box, two runs each).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void tma_load_3d_evict_first(void* dst, const CUtensorMap* map,
+                                                        uint64_t* bar, int x, int y, int z,
+                                                        uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "l"(pol)
+      : "memory");
+}
+
 // shared memory layout (offsets from a 1024-aligned base). P lives in tensor
 // memory and the output rows are written straight from registers, so all but
 // Q is K/V ring.
@@ -361,11 +381,12 @@ prefill_paged_tcgen05_kernel(const __grid_constant__ CUtensorMap qmap,
       if (lane == 0) {
         ok = qi == 0 || wait_or_abort(q_empty, (qi - 1) & 1, s_abort);
         if (ok) {
+          const uint64_t q_policy = l2_evict_first_policy();
           mbar_arrive_expect_tx(q_full, hpi * kTileBytes);
           for (int h = 0; h < hpi; ++h) {
             uint8_t* qd = smem + kOffQ + h * kTileBytes;
-            tma_load_3d(qd, &qmap, q_full, 0, h0 + h, r0);
-            tma_load_3d(qd + kHalf, &qmap, q_full, 64, h0 + h, r0);
+            tma_load_3d_evict_first(qd, &qmap, q_full, 0, h0 + h, r0, q_policy);
+            tma_load_3d_evict_first(qd + kHalf, &qmap, q_full, 64, h0 + h, r0, q_policy);
           }
         }
       }
