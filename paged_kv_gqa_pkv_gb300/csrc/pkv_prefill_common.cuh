@@ -267,35 +267,6 @@ __device__ __forceinline__ float softmax_row_to_tmem(const uint32_t (&sr)[128], 
   return (a + b) + (c + d);
 }
 
-// The epilogue of one row: O / l from this thread's TMEM lane (columns t_o ..
-// t_o + 127) as bf16 into orow (zeros when `has` is false), 32 head dims at a
-// time, straight from registers to global memory. Every lane of the warp must
-// call it (the TMEM loads are warp-collective); only lanes with `store` set
-// write.
-__device__ __forceinline__ void store_o_row(__nv_bfloat16* orow, uint32_t t_o, float inv,
-                                            bool has, bool store) {
-#pragma unroll
-  for (int c = 0; c < kHeadDim; c += 32) {
-    uint32_t o[32];
-    tmem_ld32(t_o + c, o);
-    tmem_wait_ld();
-    if (store) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if (has) {
-          const int e = 8 * q;
-          w.x = pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
-          w.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-          w.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-          w.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-        }
-        reinterpret_cast<uint4*>(orow + c)[q] = w;
-      }
-    }
-  }
-}
-
 // Bounded wait that also gives up when another role has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity,
                                               volatile int* abort_flag) {
