@@ -152,8 +152,9 @@ pkv_status decode_entry(const pkv_cache_desc* cache, const void* k_pool, const v
   // A batch past the kernels' row tables runs as consecutive launches of at
   // most kDecodeMaxBatch rows each, equal in size, on the caller's stream;
   // they reuse one workspace in stream order.
-  const int launches = (batch + pkv::kDecodeMaxBatch - 1) / pkv::kDecodeMaxBatch;
-  const int rows_per_launch = (batch + launches - 1) / launches;
+  const int64_t launches =
+      (static_cast<int64_t>(batch) + pkv::kDecodeMaxBatch - 1) / pkv::kDecodeMaxBatch;
+  const int rows_per_launch = static_cast<int>((batch + launches - 1) / launches);
   const size_t need =
       pkv::decode_workspace_bytes(rows_per_launch, cache->num_kv_heads, group, workers);
   if (workspace == nullptr || workspace_bytes < need) return PKV_ERR_WORKSPACE;
@@ -201,9 +202,9 @@ pkv_status decode_entry(const pkv_cache_desc* cache, const void* k_pool, const v
   if (launches == 1) return cuda_status(pkv::launch_decode(p, kmap, vmap, sms, stream));
   const size_t q_row = static_cast<size_t>(num_q_heads) * cache->head_dim * 2;
   const size_t kv_row = static_cast<size_t>(cache->num_kv_heads) * cache->head_dim * 2;
-  for (int r0 = 0; r0 < batch; r0 += rows_per_launch) {
+  for (int64_t r0 = 0; r0 < batch; r0 += rows_per_launch) {
     pkv::DecodeParams pr = p;
-    pr.batch = batch - r0 < rows_per_launch ? batch - r0 : rows_per_launch;
+    pr.batch = static_cast<int>(batch - r0 < rows_per_launch ? batch - r0 : rows_per_launch);
     pr.q = static_cast<const uint8_t*>(p.q) + r0 * q_row;
     pr.batch_idx = batch_idx + r0;
     pr.seq_lens = seq_lens + r0;
@@ -361,8 +362,9 @@ size_t pkv_decode_workspace_size(const pkv_cache_desc* cache, int batch, int num
   if (device_info(&sms) != PKV_OK) return 0;
   // rows of one launch: larger batches run as equal launches of at most
   // kDecodeMaxBatch rows that reuse the workspace
-  const int launches = (batch + pkv::kDecodeMaxBatch - 1) / pkv::kDecodeMaxBatch;
-  const int rows = launches > 1 ? (batch + launches - 1) / launches : batch;
+  const int64_t launches =
+      (static_cast<int64_t>(batch) + pkv::kDecodeMaxBatch - 1) / pkv::kDecodeMaxBatch;
+  const int rows = launches > 1 ? static_cast<int>((batch + launches - 1) / launches) : batch;
   return pkv::decode_workspace_bytes(rows, cache->num_kv_heads,
                                      num_q_heads / cache->num_kv_heads,
                                      pkv::decode_workers_for_device(sms));
