@@ -185,7 +185,7 @@ size_t pkv_decode_workspace_size(const pkv_cache_desc* cache, int batch,
  * workspace: device scratch of at least pkv_decode_workspace_size() bytes,
  * 256-byte aligned, owned by the caller; its contents need no initialisation
  * and are overwritten; calls that share a workspace must be stream-ordered.
- * Two kernels run: the split-KV pass and the LSE merge.
+ * Each launch runs two kernels: the split-KV pass and the LSE merge.
  */
 pkv_status pkv_decode_attention(const pkv_cache_desc* cache, const void* k_pool,
                                 const void* v_pool, const int32_t* page_table,
